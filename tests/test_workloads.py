@@ -1,0 +1,104 @@
+"""The seeded input recipe: the drawn lengths, the FP8 per-token
+quantisation, shapes and the algorithmic FLOP counts of the five workloads."""
+import json
+import math
+import os
+
+import pytest
+import torch
+
+from attention_forward_sm100_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def test_varlen_lengths_reproduce_fixture():
+    with open(os.path.join(GOLDEN, "varlen_lengths_seed2.json")) as f:
+        fx = json.load(f)
+    spec = W.WORKLOADS["varlen_gqa_b8_hq32_hkv8_d128_causal"]
+    assert list(spec.lengths_q) == fx["lengths"]
+    assert sum(spec.lengths_q) == fx["total_tokens"]
+    assert all(512 <= n <= 8192 for n in spec.lengths_q)
+
+
+def test_fp8_quantisation_properties():
+    g = torch.Generator().manual_seed(7)
+    x = torch.randn(64, 4, 128, generator=g)
+    x8, s = W.quantize_fp8_per_token(x)
+    assert x8.dtype == torch.float8_e4m3fn and s.shape == (64, 4)
+    deq = x8.float() * s.unsqueeze(-1)
+    # e4m3 keeps 3 mantissa bits: relative rounding error at most 2^-4 for
+    # normal values; subnormal codes (below 2^-6 of the range) have absolute
+    # step 2^-9 * scale.
+    err = (deq - x).abs()
+    bound = torch.maximum(x.abs() * 2.0 ** -4, s.unsqueeze(-1) * 2.0 ** -10)
+    assert bool((err <= bound + 1e-7).all())
+    # the per-vector amax maps to exactly 448
+    amax_code = x8.float().abs().amax(dim=-1)
+    assert bool((amax_code == 448.0).all())
+
+
+def test_fp8_exact_for_small_integers():
+    x = torch.tensor([[[448.0, -448.0, 1.0, 0.5, -3.0, 0.0, 96.0, 2.0]]])
+    x8, s = W.quantize_fp8_per_token(x)
+    assert s.item() == 1.0
+    assert torch.equal(x8.float(), x)
+    z8, zs = W.quantize_fp8_per_token(torch.zeros(1, 1, 8))
+    assert zs.item() == 1.0 and torch.equal(z8.float(), torch.zeros(1, 1, 8))
+
+
+@pytest.mark.parametrize("name", W.WORKLOAD_ORDER)
+def test_flops_closed_form(name):
+    spec = W.WORKLOADS[name]
+    lq, lk = spec.seq_lengths()
+    d = spec.d_qk + spec.rope + spec.d_v
+    if spec.causal:
+        pairs = sum(n * (n + 1) // 2 for n in lq)
+    else:
+        pairs = sum(a * b for a, b in zip(lq, lk))
+    assert spec.flops() == 2 * d * pairs * spec.heads_q
+
+
+def test_flops_table():
+    expect = {
+        "mha_b1_h2_s128_d64_noncausal": 8_388_608,
+        "mha_b4_h16_s4096_d128_causal": 274_945_015_808,
+        "varlen_gqa_b8_hq32_hkv8_d128_causal": 1_060_719_804_416,
+        "mla_b2_h128_s4096_d128r64_causal": 1_374_725_079_040,
+        "fp8_b2_h32_s8192_d128_causal": 1_099_645_845_504,
+    }
+    for name, f in expect.items():
+        assert W.WORKLOADS[name].flops() == f
+
+
+def test_small_inputs_shapes_and_determinism():
+    spec = W.AttnSpec(batch=2, heads_q=4, heads_kv=2, seqlen_q=9, seqlen_k=9, d_qk=64, d_v=64,
+                      causal=True, seed=11)
+    a = W.make_inputs(spec)
+    b = W.make_inputs(spec)
+    assert a["q"].shape == (2, 9, 4, 64) and a["k"].shape == (2, 9, 2, 64)
+    assert a["q"].dtype == torch.bfloat16
+    assert torch.equal(a["q"].float(), b["q"].float()) and torch.equal(a["v"].float(), b["v"].float())
+    assert math.isclose(spec.softmax_scale, 1 / 8)
+    vl = W.AttnSpec(batch=3, heads_q=2, heads_kv=1, seqlen_q=7, seqlen_k=7, d_qk=128, d_v=128,
+                    causal=True, seed=3, lengths_q=(7, 1, 4))
+    c = W.make_inputs(vl)
+    assert c["q"].shape == (12, 2, 128) and c["cu_seqlens_q"].tolist() == [0, 7, 8, 12]
+    f8 = W.AttnSpec(batch=1, heads_q=2, heads_kv=2, seqlen_q=5, seqlen_k=5, d_qk=128, d_v=128,
+                    causal=True, seed=4, qk_dtype="fp8")
+    d = W.make_inputs(f8)
+    assert d["q"].dtype == torch.float8_e4m3fn and d["q_scale"].shape == (1, 2, 5)
+    ml = W.AttnSpec(batch=1, heads_q=2, heads_kv=2, seqlen_q=5, seqlen_k=5, d_qk=128, d_v=128,
+                    causal=True, seed=4, rope=64)
+    e = W.make_inputs(ml)
+    assert e["k_rope"].shape == (1, 5, 64) and e["q_rope"].shape == (1, 5, 2, 64)
+    assert math.isclose(ml.softmax_scale, 1 / math.sqrt(192))
+
+
+def test_sample_rows_in_range():
+    spec = W.WORKLOADS["varlen_gqa_b8_hq32_hkv8_d128_causal"]
+    rows = W.sample_rows(spec, 256, 102)
+    lq, _ = spec.seq_lengths()
+    assert len(rows) == 260
+    for b, h, i in rows:
+        assert 0 <= b < spec.batch and 0 <= h < spec.heads_q and 0 <= i < lq[b]
