@@ -1,0 +1,12 @@
+"""GB300 (sm_103a) fused attention forward: a C-ABI CUDA library and its
+Python binding.
+
+``forward`` computes O = softmax(scale * Q K^T + causal mask) V and the per-row
+log-sum-exp with one persistent tcgen05/TMA kernel. Build the library with
+``attention_forward_sm100_gb300.build.build()``.
+"""
+from ._binding import (AttnError, Params, PlanInfo, check, default_workspace, forward, last_error, lib,
+                       make_params, plan, schedule)
+
+__all__ = ["AttnError", "Params", "PlanInfo", "check", "default_workspace", "forward", "last_error", "lib",
+           "make_params", "plan", "schedule"]

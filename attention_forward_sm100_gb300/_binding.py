@@ -1,0 +1,253 @@
+"""ctypes binding of libattn_fwd.so (argument marshalling only).
+
+Every step of the attention forward runs in the library's CUDA kernels; this
+module only turns torch tensors into the pointers, sizes and strides of
+``attn_fwd_params`` and raises when the library is missing or refuses the
+call. There is no CPU path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn_fwd.so")
+
+ATTN_OK = 0
+STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "cuda error", 4: "device timeout"}
+BACKENDS = {"tcgen05": 0, "simple": 1}
+DTYPES = {torch.bfloat16: 0, torch.float8_e4m3fn: 1}
+WORKSPACE_BYTES = 256
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__(f"attn_fwd: {STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class Params(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("q_rope", ctypes.c_void_p), ("k_rope", ctypes.c_void_p),
+        ("q_scale", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+        ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p),
+        ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("batch", ctypes.c_int32), ("seqlen_q", ctypes.c_int32), ("seqlen_k", ctypes.c_int32),
+        ("total_q", ctypes.c_int32), ("total_k", ctypes.c_int32),
+        ("num_heads_q", ctypes.c_int32), ("num_heads_kv", ctypes.c_int32),
+        ("head_dim_qk", ctypes.c_int32), ("head_dim_v", ctypes.c_int32), ("rope_depth", ctypes.c_int32),
+        ("causal", ctypes.c_int32), ("softmax_scale", ctypes.c_float),
+        ("qk_dtype", ctypes.c_int32), ("backend", ctypes.c_int32),
+        ("q_stride", ctypes.c_int64 * 3), ("k_stride", ctypes.c_int64 * 3), ("v_stride", ctypes.c_int64 * 3),
+        ("o_stride", ctypes.c_int64 * 3), ("q_rope_stride", ctypes.c_int64 * 3),
+        ("k_rope_stride", ctypes.c_int64 * 2),
+    ]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("backend", ctypes.c_int32), ("rows_per_tile", ctypes.c_int32), ("work_tiles", ctypes.c_int64),
+                ("grid", ctypes.c_int32), ("block", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
+                ("k_stages", ctypes.c_int32), ("v_stages", ctypes.c_int32), ("tmem_columns", ctypes.c_int32)]
+
+
+class WorkTile(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("head", ctypes.c_int32), ("tile", ctypes.c_int32)]
+
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lib_lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is not built: run attention_forward_sm100_gb300.build.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            L.attn_fwd.argtypes = [ctypes.POINTER(Params), ctypes.c_void_p]
+            L.attn_fwd.restype = ctypes.c_int
+            L.attn_fwd_check.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+            L.attn_fwd_check.restype = ctypes.c_int
+            L.attn_fwd_plan.argtypes = [ctypes.POINTER(Params), ctypes.POINTER(PlanInfo)]
+            L.attn_fwd_plan.restype = ctypes.c_int
+            L.attn_fwd_schedule.argtypes = [ctypes.POINTER(Params), ctypes.c_void_p, ctypes.POINTER(WorkTile),
+                                            ctypes.c_int64]
+            L.attn_fwd_schedule.restype = ctypes.c_int64
+            L.attn_fwd_workspace_bytes.argtypes = [ctypes.POINTER(Params)]
+            L.attn_fwd_workspace_bytes.restype = ctypes.c_size_t
+            L.attn_fwd_params_init.argtypes = [ctypes.POINTER(Params)]
+            L.attn_fwd_params_init.restype = None
+            L.attn_fwd_params_size.argtypes = []
+            L.attn_fwd_params_size.restype = ctypes.c_size_t
+            L.attn_status_string.argtypes = [ctypes.c_int]
+            L.attn_status_string.restype = ctypes.c_char_p
+            L.attn_fwd_last_error.argtypes = []
+            L.attn_fwd_last_error.restype = ctypes.c_char_p
+            if L.attn_fwd_params_size() != ctypes.sizeof(Params):
+                raise RuntimeError("attn_fwd_params layout mismatch between the binding and the library")
+            _lib = L
+    return _lib
+
+
+def last_error() -> str:
+    return lib().attn_fwd_last_error().decode()
+
+
+_workspaces = {}
+
+
+def default_workspace(device) -> torch.Tensor:
+    """A zero-filled workspace per device (the library keeps it zeroed)."""
+    device = torch.device(device)
+    key = (device.type, device.index)
+    ws = _workspaces.get(key)
+    if ws is None:
+        ws = torch.zeros(WORKSPACE_BYTES, dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _require_cuda(name, t):
+    if t is not None and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (this library has no CPU path)")
+
+
+def make_params(q, k, v, *, causal, softmax_scale=None, q_rope=None, k_rope=None, q_scale=None, k_scale=None,
+                cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, out=None, lse=None,
+                workspace=None, backend="tcgen05") -> Params:
+    """attn_fwd_params for torch tensors (shapes are read, nothing is allocated)."""
+    packed = cu_seqlens_q is not None
+    p = Params()
+    if packed:
+        tq, hq, d = q.shape
+        tk, hkv, _ = k.shape
+        b = cu_seqlens_q.numel() - 1
+        p.total_q, p.total_k = tq, tk
+        p.seqlen_q = int(max_seqlen_q if max_seqlen_q is not None else tq)
+        p.seqlen_k = int(max_seqlen_k if max_seqlen_k is not None else tk)
+    else:
+        b, sq, hq, d = q.shape
+        _, sk, hkv, _ = k.shape
+        p.seqlen_q, p.seqlen_k = sq, sk
+    rope = 0 if q_rope is None else q_rope.shape[-1]
+    p.batch, p.num_heads_q, p.num_heads_kv = b, hq, hkv
+    p.head_dim_qk, p.head_dim_v, p.rope_depth = d, v.shape[-1], rope
+    p.causal = 1 if causal else 0
+    p.softmax_scale = float(softmax_scale if softmax_scale is not None else (d + rope) ** -0.5)
+    if q.dtype not in DTYPES:
+        raise ValueError(f"unsupported q dtype {q.dtype}")
+    p.qk_dtype = DTYPES[q.dtype]
+    p.backend = BACKENDS[backend]
+    p.q, p.k, p.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
+    p.q_rope, p.k_rope = _ptr(q_rope), _ptr(k_rope)
+    p.q_scale, p.k_scale = _ptr(q_scale), _ptr(k_scale)
+    p.cu_seqlens_q, p.cu_seqlens_k = _ptr(cu_seqlens_q), _ptr(cu_seqlens_k)
+    p.o = _ptr(out)
+    p.lse = _ptr(lse)
+    if workspace is not None:
+        p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+    def strides3(t):
+        s = t.stride()
+        return (0, s[0], s[1]) if packed else (s[0], s[1], s[2])
+
+    p.q_stride[:] = strides3(q)
+    p.k_stride[:] = strides3(k)
+    p.v_stride[:] = strides3(v)
+    if out is not None:
+        p.o_stride[:] = strides3(out)
+    if q_rope is not None:
+        p.q_rope_stride[:] = strides3(q_rope)
+        s = k_rope.stride()
+        p.k_rope_stride[:] = (0, s[0]) if packed else (s[0], s[1])
+    return p
+
+
+def forward(q, k, v, *, causal=False, softmax_scale=None, q_rope=None, k_rope=None, q_scale=None, k_scale=None,
+            cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, out=None, lse=None,
+            return_lse=True, workspace=None, backend="tcgen05", stream=None):
+    """Fused attention forward on the GPU; returns (O, LSE).
+
+    Fixed length: q [B,Sq,Hq,D], k [B,Sk,Hkv,D], v [B,Sk,Hkv,Dv] -> O
+    [B,Sq,Hq,Dv] bf16, LSE [B,Hq,Sq] fp32. Packed: q [Tq,Hq,D] etc. with int32
+    cu_seqlens_q / cu_seqlens_k -> O [Tq,Hq,Dv], LSE [Hq,Tq]. Optional rope
+    parts q_rope [..,Hq,R] and k_rope [..,R] (one per token, shared by heads);
+    fp8 e4m3 q/k need per-token fp32 scales q_scale [B,Hq,Sq] / [Hq,Tq] and
+    k_scale [B,Hkv,Sk] / [Hkv,Tk]. Asynchronous on ``stream`` (default: the
+    current torch stream).
+    """
+    for name, t in (("q", q), ("k", k), ("v", v), ("q_rope", q_rope), ("k_rope", k_rope), ("q_scale", q_scale),
+                    ("k_scale", k_scale), ("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        _require_cuda(name, t)
+    L = lib()
+    packed = cu_seqlens_q is not None
+    dev = q.device
+    if out is None:
+        out = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=torch.bfloat16, device=dev)
+    if lse is None and return_lse:
+        if packed:
+            lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=dev)
+        else:
+            lse = torch.empty((q.shape[0], q.shape[2], q.shape[1]), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = default_workspace(dev)
+    p = make_params(q, k, v, causal=causal, softmax_scale=softmax_scale, q_rope=q_rope, k_rope=k_rope,
+                    q_scale=q_scale, k_scale=k_scale, cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k,
+                    max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k, out=out, lse=lse,
+                    workspace=workspace, backend=backend)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    st = L.attn_fwd(ctypes.byref(p), ctypes.c_void_p(handle))
+    if st != ATTN_OK:
+        raise AttnError(st, last_error())
+    return out, lse
+
+
+def check(workspace=None, device=None, stream=None):
+    """Synchronises and raises if a kernel wait ran out of time."""
+    L = lib()
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    ws = workspace if workspace is not None else default_workspace(dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    st = L.attn_fwd_check(ctypes.c_void_p(ws.data_ptr()), ctypes.c_void_p(handle))
+    if st != ATTN_OK:
+        raise AttnError(st, last_error())
+
+
+def plan(p: Params) -> PlanInfo:
+    info = PlanInfo()
+    st = lib().attn_fwd_plan(ctypes.byref(p), ctypes.byref(info))
+    if st != ATTN_OK:
+        raise AttnError(st, last_error())
+    return info
+
+
+def schedule(p: Params, host_cu_seqlens_q=None):
+    """The persistent scheduler's order of work tiles, as (batch, head, tile)."""
+    L = lib()
+    cu = None
+    cu_arr = None
+    if host_cu_seqlens_q is not None:
+        cu_arr = (ctypes.c_int32 * len(host_cu_seqlens_q))(*[int(x) for x in host_cu_seqlens_q])
+        cu = ctypes.cast(cu_arr, ctypes.c_void_p)
+    n = L.attn_fwd_schedule(ctypes.byref(p), cu, None, 0)
+    if n < 0:
+        raise AttnError(1, "bad schedule arguments")
+    out = (WorkTile * max(n, 1))()
+    L.attn_fwd_schedule(ctypes.byref(p), cu, out, n)
+    return [(w.batch, w.head, w.tile) for w in out[:n]]

@@ -1,0 +1,362 @@
+// Host side of the C ABI declared in include/attn_fwd.h: argument validation,
+// launch planning, TMA descriptor encoding and kernel dispatch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "internal.h"
+#include "schedule.cuh"
+
+namespace {
+
+thread_local char g_last_error[512] = {0};
+
+attn_status fail(attn_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+void clear_error() { g_last_error[0] = 0; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int qk_elem_bytes(const attn_fwd_params* p) { return p->qk_dtype == ATTN_DTYPE_FP8_E4M3 ? 1 : 2; }
+
+// ---------------------------------------------------------------- validation
+attn_status validate(const attn_fwd_params* p) {
+  if (p == nullptr) return fail(ATTN_ERR_INVALID_ARG, "params is NULL");
+  if (p->qk_dtype != ATTN_DTYPE_BF16 && p->qk_dtype != ATTN_DTYPE_FP8_E4M3)
+    return fail(ATTN_ERR_INVALID_ARG, "unknown qk_dtype %d", p->qk_dtype);
+  if (p->backend != ATTN_BACKEND_TCGEN05 && p->backend != ATTN_BACKEND_SIMPLE)
+    return fail(ATTN_ERR_INVALID_ARG, "unknown backend %d", p->backend);
+  if (p->batch < 0 || p->seqlen_q < 0 || p->seqlen_k < 0 || p->total_q < 0 || p->total_k < 0)
+    return fail(ATTN_ERR_INVALID_ARG, "negative size");
+  if (p->num_heads_q <= 0 || p->num_heads_kv <= 0)
+    return fail(ATTN_ERR_INVALID_ARG, "head counts must be positive");
+  if (p->num_heads_q % p->num_heads_kv != 0)
+    return fail(ATTN_ERR_INVALID_ARG, "num_heads_q %d is not a multiple of num_heads_kv %d",
+                p->num_heads_q, p->num_heads_kv);
+  if (p->head_dim_qk <= 0 || p->head_dim_v <= 0 || p->rope_depth < 0)
+    return fail(ATTN_ERR_INVALID_ARG, "head dims must be positive");
+  if (!(p->softmax_scale > 0.f) || p->softmax_scale != p->softmax_scale)
+    return fail(ATTN_ERR_INVALID_ARG, "softmax_scale must be a positive number");
+  const bool packed = p->cu_seqlens_q != nullptr;
+  if (packed != (p->cu_seqlens_k != nullptr))
+    return fail(ATTN_ERR_INVALID_ARG, "cu_seqlens_q and cu_seqlens_k must both be set or both NULL");
+  if (packed && ((reinterpret_cast<uintptr_t>(p->cu_seqlens_q) | reinterpret_cast<uintptr_t>(p->cu_seqlens_k)) & 3))
+    return fail(ATTN_ERR_INVALID_ARG, "cu_seqlens must be 4-byte aligned");
+  if (packed && (p->total_q <= 0 && p->batch > 0 && p->seqlen_q > 0))
+    return fail(ATTN_ERR_INVALID_ARG, "packed layout needs total_q");
+  if (p->q == nullptr || p->k == nullptr || p->v == nullptr || p->o == nullptr)
+    return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be non-NULL");
+  if (p->rope_depth > 0 && (p->q_rope == nullptr || p->k_rope == nullptr))
+    return fail(ATTN_ERR_INVALID_ARG, "rope_depth > 0 needs q_rope and k_rope");
+  if (p->qk_dtype == ATTN_DTYPE_FP8_E4M3) {
+    if (p->q_scale == nullptr || p->k_scale == nullptr)
+      return fail(ATTN_ERR_INVALID_ARG, "fp8 Q/K need q_scale and k_scale");
+    if (p->rope_depth > 0) return fail(ATTN_ERR_UNSUPPORTED, "fp8 Q/K with a rope part");
+  }
+  for (int i = 0; i < 3; ++i) {
+    if (p->q_stride[i] < 0 || p->k_stride[i] < 0 || p->v_stride[i] < 0 || p->o_stride[i] < 0 ||
+        p->q_rope_stride[i] < 0)
+      return fail(ATTN_ERR_INVALID_ARG, "negative stride");
+  }
+  if (p->backend == ATTN_BACKEND_TCGEN05) {
+    if (p->workspace == nullptr || p->workspace_bytes < ATTN_FWD_WORKSPACE_BYTES)
+      return fail(ATTN_ERR_INVALID_ARG, "workspace of at least %d bytes is required", ATTN_FWD_WORKSPACE_BYTES);
+    if (reinterpret_cast<uintptr_t>(p->workspace) & 255u)
+      return fail(ATTN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    // TMA: 16-byte aligned bases and strides that are multiples of 16 bytes.
+    const int es = qk_elem_bytes(p);
+    if (!aligned16(p->q) || !aligned16(p->k) || !aligned16(p->v))
+      return fail(ATTN_ERR_INVALID_ARG, "q, k, v must be 16-byte aligned");
+    for (int i = packed ? 1 : 0; i < 3; ++i) {
+      if ((p->q_stride[i] * es) % 16 || (p->k_stride[i] * es) % 16 || (p->v_stride[i] * 2) % 16)
+        return fail(ATTN_ERR_INVALID_ARG, "q/k/v strides must be multiples of 16 bytes");
+    }
+    if (p->rope_depth > 0) {
+      if (!aligned16(p->q_rope) || !aligned16(p->k_rope))
+        return fail(ATTN_ERR_INVALID_ARG, "q_rope, k_rope must be 16-byte aligned");
+      for (int i = packed ? 1 : 0; i < 3; ++i)
+        if ((p->q_rope_stride[i] * 2) % 16) return fail(ATTN_ERR_INVALID_ARG, "q_rope strides must be multiples of 16 bytes");
+      for (int i = packed ? 1 : 0; i < 2; ++i)
+        if ((p->k_rope_stride[i] * 2) % 16) return fail(ATTN_ERR_INVALID_ARG, "k_rope strides must be multiples of 16 bytes");
+    }
+    if ((p->o_stride[2] * 2) % 16 || (p->o_stride[1] * 2) % 16 || !aligned16(p->o))
+      return fail(ATTN_ERR_INVALID_ARG, "o must be 16-byte aligned with 16-byte multiple strides");
+    const bool ok_bf16 = p->qk_dtype == ATTN_DTYPE_BF16 &&
+        ((p->head_dim_qk == 64 && p->head_dim_v == 64 && p->rope_depth == 0) ||
+         (p->head_dim_qk == 128 && p->head_dim_v == 128 && (p->rope_depth == 0 || p->rope_depth == 64)));
+    const bool ok_fp8 = p->qk_dtype == ATTN_DTYPE_FP8_E4M3 && p->head_dim_qk == 128 &&
+                        p->head_dim_v == 128 && p->rope_depth == 0;
+    if (!ok_bf16 && !ok_fp8)
+      return fail(ATTN_ERR_UNSUPPORTED, "tcgen05 kernel supports (Dqk,Dv,R) = (64,64,0), (128,128,0), "
+                  "(128,128,64) for bf16 and (128,128,0) for fp8; got (%d,%d,%d)",
+                  p->head_dim_qk, p->head_dim_v, p->rope_depth);
+  } else {
+    if (p->head_dim_qk + p->rope_depth > 256 || p->head_dim_v > 256)
+      return fail(ATTN_ERR_UNSUPPORTED, "simple kernel supports Dqk + R <= 256 and Dv <= 256");
+  }
+  return ATTN_OK;
+}
+
+int tc05_variant(const attn_fwd_params* p) {
+  if (p->qk_dtype == ATTN_DTYPE_FP8_E4M3) return af::kVarFp8D128;
+  if (p->head_dim_qk == 64) return af::kVarD64;
+  return p->rope_depth ? af::kVarD128Rope64 : af::kVarD128;
+}
+
+int sm_count_cached() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 148;
+  }
+  if (dev < 0 || dev >= 64) return 148;
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+    cudaGetLastError();
+    return 148;
+  }
+  cache[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+int64_t work_tiles_bound(const attn_fwd_params* p) {
+  const int64_t T = af::tiles_for(p->seqlen_q, af::kRowsPerTile);
+  return (int64_t)p->batch * p->num_heads_q * T;
+}
+
+// ---------------------------------------------------------------- tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// 4-D map over (depth, head, token, batch); box {box_d, 1, 128, 1}, 128-byte swizzle.
+attn_status make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int es, int64_t depth,
+                     int64_t heads, int64_t tokens, int64_t batches, int64_t sh, int64_t st, int64_t sb,
+                     int box_d) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
+  if (heads <= 1) sh = st > 0 ? st : depth;   // a size-1 dimension: any legal stride
+  if (batches <= 1) sb = st * (tokens > 0 ? tokens : 1);
+  if (tokens < 1) tokens = 1;
+  cuuint64_t dims[4] = {(cuuint64_t)depth, (cuuint64_t)heads, (cuuint64_t)tokens, (cuuint64_t)batches};
+  cuuint64_t strides[3] = {(cuuint64_t)(sh * es), (cuuint64_t)(st * es), (cuuint64_t)(sb * es)};
+  cuuint32_t box[4] = {(cuuint32_t)box_d, 1u, (cuuint32_t)af::kBlockN, 1u};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUresult r = fn(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(ATTN_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (%d) for a %lldx%lldx%lldx%lld tensor", (int)r,
+                (long long)depth, (long long)heads, (long long)tokens, (long long)batches);
+  return ATTN_OK;
+}
+
+attn_status launch_tc05(const attn_fwd_params* p, cudaStream_t stream) {
+  const bool packed = p->cu_seqlens_q != nullptr;
+  const int variant = tc05_variant(p);
+  af::Tc05Params prm;
+  memset(&prm, 0, sizeof(prm));
+  const bool fp8 = p->qk_dtype == ATTN_DTYPE_FP8_E4M3;
+  const CUtensorMapDataType qk_t = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int es = fp8 ? 1 : 2;
+  const int box_qk = fp8 ? 128 : 64;
+  const int64_t tq = packed ? p->total_q : p->seqlen_q, tk = packed ? p->total_k : p->seqlen_k;
+  const int64_t nb = packed ? 1 : p->batch;
+  attn_status st;
+  if ((st = make_map(&prm.tm_q, p->q, qk_t, es, p->head_dim_qk, p->num_heads_q, tq, nb, p->q_stride[2],
+                     p->q_stride[1], p->q_stride[0], box_qk)) != ATTN_OK)
+    return st;
+  if ((st = make_map(&prm.tm_k, p->k, qk_t, es, p->head_dim_qk, p->num_heads_kv, tk, nb, p->k_stride[2],
+                     p->k_stride[1], p->k_stride[0], box_qk)) != ATTN_OK)
+    return st;
+  if ((st = make_map(&prm.tm_v, p->v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->head_dim_v, p->num_heads_kv, tk, nb,
+                     p->v_stride[2], p->v_stride[1], p->v_stride[0], 64)) != ATTN_OK)
+    return st;
+  if (p->rope_depth > 0) {
+    if ((st = make_map(&prm.tm_qr, p->q_rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->rope_depth, p->num_heads_q,
+                       tq, nb, p->q_rope_stride[2], p->q_rope_stride[1], p->q_rope_stride[0], 64)) != ATTN_OK)
+      return st;
+    if ((st = make_map(&prm.tm_kr, p->k_rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->rope_depth, 1, tk, nb,
+                       p->k_rope_stride[1], p->k_rope_stride[1], p->k_rope_stride[0], 64)) != ATTN_OK)
+      return st;
+  }
+  prm.q_scale = p->q_scale;
+  prm.k_scale = p->k_scale;
+  prm.cu_q = p->cu_seqlens_q;
+  prm.cu_k = p->cu_seqlens_k;
+  prm.o = static_cast<uint16_t*>(p->o);
+  prm.lse = p->lse;
+  prm.ws = static_cast<uint32_t*>(p->workspace);
+  prm.o_stride_b = packed ? 0 : p->o_stride[0];
+  prm.o_stride_t = p->o_stride[1];
+  prm.o_stride_h = p->o_stride[2];
+  prm.batch = p->batch;
+  prm.seqlen_q = p->seqlen_q;
+  prm.seqlen_k = p->seqlen_k;
+  prm.heads_q = p->num_heads_q;
+  prm.heads_kv = p->num_heads_kv;
+  prm.group = p->num_heads_q / p->num_heads_kv;
+  prm.tiles_per_seq = af::tiles_for(p->seqlen_q, af::kRowsPerTile);
+  prm.total_work = packed ? 0 : work_tiles_bound(p);
+  prm.packed = packed ? 1 : 0;
+  prm.total_q = packed ? p->total_q : 0;
+  prm.total_k = packed ? p->total_k : 0;
+  prm.scale_log2 = p->softmax_scale * 1.4426950408889634f;
+  int64_t bound = work_tiles_bound(p);
+  if (bound <= 0) return ATTN_OK;
+  const int grid = (int)(bound < sm_count_cached() ? bound : sm_count_cached());
+  cudaError_t e = af::tc05_launch(variant, p->causal != 0, prm, grid, stream);
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "tcgen05 kernel launch failed: %s", cudaGetErrorString(e));
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void attn_fwd_params_init(attn_fwd_params* p) {
+  if (p == nullptr) return;
+  memset(p, 0, sizeof(*p));
+  p->qk_dtype = ATTN_DTYPE_BF16;
+  p->backend = ATTN_BACKEND_TCGEN05;
+  p->softmax_scale = 1.f;
+}
+
+size_t attn_fwd_workspace_bytes(const attn_fwd_params* p) {
+  (void)p;
+  return ATTN_FWD_WORKSPACE_BYTES;
+}
+
+size_t attn_fwd_params_size(void) { return sizeof(attn_fwd_params); }
+
+attn_status attn_fwd(const attn_fwd_params* p, attn_stream_t stream) {
+  clear_error();
+  attn_status st = validate(p);
+  if (st != ATTN_OK) return st;
+  if (p->batch == 0 || p->seqlen_q == 0) return ATTN_OK;
+  if (p->cu_seqlens_q != nullptr && p->total_q == 0) return ATTN_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p->backend == ATTN_BACKEND_SIMPLE) {
+    cudaError_t e = af::simple_launch(*p, s);
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "simple kernel launch failed: %s", cudaGetErrorString(e));
+    return ATTN_OK;
+  }
+  return launch_tc05(p, s);
+}
+
+attn_status attn_fwd_check(void* workspace, attn_stream_t stream) {
+  clear_error();
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "stream error: %s", cudaGetErrorString(e));
+  if (workspace == nullptr) return ATTN_OK;
+  uint32_t w[af::kWsWords];
+  e = cudaMemcpy(w, workspace, sizeof(w), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "reading the workspace failed: %s", cudaGetErrorString(e));
+  if (w[af::kWsErrorCode] != af::kDevErrNone) {
+    const uint32_t info = w[af::kWsErrorInfo];
+    cudaMemset(static_cast<uint32_t*>(workspace) + af::kWsErrorCode, 0, 2 * sizeof(uint32_t));
+    cudaDeviceSynchronize();
+    return fail(ATTN_ERR_DEVICE_TIMEOUT, "device wait timed out (code %u, block %u, role %u, barrier %u)",
+                w[af::kWsErrorCode], info >> 16, (info >> 8) & 0xffu, info & 0xffu);
+  }
+  return ATTN_OK;
+}
+
+attn_status attn_fwd_plan(const attn_fwd_params* p, attn_fwd_plan_info* out) {
+  clear_error();
+  if (out == nullptr) return fail(ATTN_ERR_INVALID_ARG, "out is NULL");
+  attn_status st = validate(p);
+  if (st != ATTN_OK) return st;
+  memset(out, 0, sizeof(*out));
+  out->backend = p->backend;
+  if (p->backend == ATTN_BACKEND_SIMPLE) {
+    out->rows_per_tile = 4;
+    out->work_tiles = (int64_t)((p->seqlen_q + 3) / 4) * p->num_heads_q * p->batch;
+    out->grid = (int32_t)out->work_tiles;
+    out->block = 128;
+    return ATTN_OK;
+  }
+  const af::Tc05Config c = af::tc05_config(tc05_variant(p));
+  out->rows_per_tile = af::kRowsPerTile;
+  out->work_tiles = work_tiles_bound(p);
+  const int sms = sm_count_cached();
+  out->grid = (int32_t)(out->work_tiles < sms ? out->work_tiles : sms);
+  out->block = c.threads;
+  out->smem_bytes = c.smem_bytes;
+  out->k_stages = c.k_stages;
+  out->v_stages = c.v_stages;
+  out->tmem_columns = c.tmem_cols;
+  return ATTN_OK;
+}
+
+int64_t attn_fwd_schedule(const attn_fwd_params* p, const int32_t* host_cu_seqlens_q, attn_work_tile* out,
+                          int64_t cap) {
+  clear_error();
+  if (p == nullptr || p->num_heads_kv <= 0 || p->num_heads_q % p->num_heads_kv) return -1;
+  const int group = p->num_heads_q / p->num_heads_kv;
+  int64_t n = 0;
+  auto emit = [&](const af::WorkTile& w) {
+    if (n < cap && out != nullptr) {
+      out[n].batch = w.b;
+      out[n].head = w.h;
+      out[n].tile = w.t;
+    }
+    ++n;
+  };
+  if (host_cu_seqlens_q == nullptr) {
+    const int32_t T = af::tiles_for(p->seqlen_q, af::kRowsPerTile);
+    const int64_t total = (int64_t)p->batch * p->num_heads_q * T;
+    for (int64_t w = 0; w < total; ++w) emit(af::decode_fixed(w, T, p->num_heads_q, group));
+    return n;
+  }
+  for (int b = 0; b < p->batch; ++b) {
+    const int32_t len = host_cu_seqlens_q[b + 1] - host_cu_seqlens_q[b];
+    const int32_t T = af::tiles_for(len, af::kRowsPerTile);
+    for (int64_t wl = 0; wl < (int64_t)T * p->num_heads_q; ++wl) emit(af::decode_in_sequence(wl, b, T, group));
+  }
+  return n;
+}
+
+const char* attn_status_string(attn_status s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* attn_fwd_last_error(void) { return g_last_error; }
+
+}  // extern "C"

@@ -1,0 +1,916 @@
+// Persistent, warp-specialised attention forward for sm_103a (tcgen05 + TMA).
+//
+// Design (prior art: the SM100 flash-attention pages "SM100AttentionSMem",
+// "TMAProducerPipeline" and "MHATileScheduler"; rebuilt here for one GB300
+// CTA per SM):
+//   * a work tile is 256 query rows of one (sequence, head), split into two
+//     128-row Q tiles that ping-pong between two softmax warpgroups so the
+//     tensor core always has one Q tile's MMAs to run while the other tile's
+//     softmax runs;
+//   * warp 13 is the scheduler and the Q/K producer: it takes work indices
+//     from an atomic counter, publishes each decoded work tile through a
+//     two-slot shared-memory ring (the shared work index of the scheduler
+//     page, initial_state / advance) and streams K tiles into a staged ring
+//     with TMA and transaction-count mbarriers (acquire / expect-bytes /
+//     commit of the producer-pipeline page); warp 14 streams V tiles into
+//     their own ring. K is stored k-major and V mn-major, both with the
+//     128-byte swizzle, exactly as the MMAs read them;
+//   * warp 12 issues every tcgen05.mma from one thread: S_i = Q_i K^T into
+//     tensor memory (fp32), then O_i += P_i V with P_i (bf16) read from tensor
+//     memory where the softmax left it, over the S_i columns;
+//   * warpgroups 0 and 1 own Q tiles 0 and 1: thread r owns row r (TMEM lane
+//     r), loads S, applies the causal / sequence-end mask, keeps the running
+//     max m and sum l in log2 units, writes P = 2^(s*c - m) as bf16 back to
+//     tensor memory and passes the rescale factor alpha through shared
+//     memory (the correction region of the layout page). The running max is
+//     only moved when it grows by more than 2^8, so most tiles need no
+//     rescale; O and l stay consistent because both use the same max;
+//   * warpgroup 2 rescales O_i in tensor memory when alpha != 1 and, after
+//     the last P V, normalises O by 1/l, rounds once to bf16 and stores it.
+// Every wait is bounded: on timeout the CTA records an error in the
+// workspace, raises a shared abort flag that all waits poll, drains its
+// outstanding copies and MMAs, frees tensor memory and exits.
+#pragma once
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "schedule.cuh"
+
+namespace af {
+
+constexpr uint32_t kFull = 0xffffffffu;
+constexpr uint64_t kTimeoutNs = 2000000000ull;   // 2 s per wait
+constexpr uint64_t kDrainTimeoutNs = 100000000ull;
+
+enum Role : int { kRoleSoftmax0 = 0, kRoleSoftmax1 = 1, kRoleCorrection = 2, kRoleMma = 3, kRoleLoadQK = 4,
+                  kRoleLoadV = 5 };
+
+enum BarId : int {
+  BAR_Q_FULL = 0,        // +i, TMA transaction barrier of Q tile i
+  BAR_Q_EMPTY = 2,       // last S MMA of a work tile done: Q region free
+  BAR_S_FULL = 3,        // +i, S_i = Q_i K^T complete
+  BAR_P_FULL = 5,        // +i, P_i written to tensor memory (128 arrivals)
+  BAR_ALPHA = 7,         // +i, alpha (or the final 1/l) of Q tile i in shared memory (128)
+  BAR_O_CORR = 9,        // +i, O_i rescaled for the next P V (128)
+  BAR_O_FINAL = 11,      // +i, last P_i V of a work tile complete
+  BAR_O_FREE = 13,       // +i, epilogue finished reading O_i (128)
+  BAR_STATS_FREE = 15,   // +i, correction read the 1/l of Q tile i (128)
+  BAR_KS = 17,           // +i, fp8 k-scale tile written by the softmax warpgroup (128)
+  BAR_SCHED_FULL = 19,   // +slot
+  BAR_SCHED_EMPTY = 21,  // +slot
+  BAR_DRAIN = 23,        // final commit of the MMA thread
+  BAR_FIXED = 24         // then K_FULL[NK], K_EMPTY[NK], V_FULL[NV], V_EMPTY[NV]
+};
+
+// Consumers of a scheduler slot: MMA lane, 2 softmax warpgroups, the
+// correction warpgroup and the V producer lane.
+constexpr uint32_t kSchedConsumers = 1 + 128 + 128 + 128 + 1;
+
+template <int DQK_, int DR_, int DV_, bool FP8_>
+struct Tc05Traits {
+  static constexpr int DQK = DQK_, DR = DR_, DV = DV_;
+  static constexpr bool FP8 = FP8_;
+  static constexpr int BM = kBlockM, BN = kBlockN, NQ = 2;
+  static constexpr int QK_CHUNK_ELEMS = FP8 ? 128 : 64;   // elements of one 128-byte swizzle row
+  static constexpr int QK_CHUNKS = DQK / QK_CHUNK_ELEMS;
+  static constexpr int R_CHUNKS = DR / 64;
+  static constexpr int V_CHUNKS = DV / 64;
+  static constexpr int CHUNK_BYTES = 128 * 128;           // 128 rows x 128 bytes
+  static constexpr int Q_TILE_BYTES = (QK_CHUNKS + R_CHUNKS) * CHUNK_BYTES;
+  static constexpr int K_STAGE_BYTES = (QK_CHUNKS + R_CHUNKS) * CHUNK_BYTES;
+  static constexpr int V_STAGE_BYTES = V_CHUNKS * CHUNK_BYTES;
+  static constexpr int NK = DR > 0 ? 2 : (FP8 ? 4 : (DQK == 64 ? 4 : 3));
+  static constexpr int NV = DR > 0 ? 1 : (FP8 ? 3 : (DQK == 64 ? 4 : 2));
+
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = NQ * Q_TILE_BYTES;
+  static constexpr int OFF_V = OFF_K + NK * K_STAGE_BYTES;
+  static constexpr int OFF_ALPHA = OFF_V + NV * V_STAGE_BYTES;      // float [NQ][BM]
+  static constexpr int OFF_RCPL = OFF_ALPHA + NQ * BM * 4;          // float [NQ][BM]
+  static constexpr int OFF_KS = OFF_RCPL + NQ * BM * 4;             // float [NQ][2][BN] (fp8)
+  static constexpr int KS_BYTES = FP8 ? NQ * 2 * BN * 4 : 0;
+  static constexpr int OFF_SCHED = OFF_KS + KS_BYTES;               // 2 slots x 32 bytes
+  static constexpr int OFF_BAR = OFF_SCHED + 64;
+  static constexpr int NUM_BARS = BAR_FIXED + 2 * NK + 2 * NV;
+  static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
+  static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
+  static constexpr int SMEM_BYTES = OFF_ABORT + 12;
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA exceeded");
+  static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+
+  static constexpr int BAR_K_FULL = BAR_FIXED;
+  static constexpr int BAR_K_EMPTY = BAR_FIXED + NK;
+  static constexpr int BAR_V_FULL = BAR_FIXED + 2 * NK;
+  static constexpr int BAR_V_EMPTY = BAR_FIXED + 2 * NK + NV;
+
+  static constexpr uint32_t TMEM_COLS = 512;
+  // Tensor-memory columns: S_0, S_1 (P_i overwrites the first 64 columns of
+  // S_i as packed bf16 pairs), O_0, O_1.
+  __host__ __device__ static constexpr uint32_t tm_s(int i) { return i ? 128u : 0u; }
+  __host__ __device__ static constexpr uint32_t tm_o(int i) { return i ? 384u : 256u; }
+
+  static constexpr uint32_t IDESC_S =
+      FP8 ? ptx::idesc_f32acc(0, 0, false, false, 128, 128) : ptx::idesc_f32acc(1, 1, false, false, 128, 128);
+  static constexpr uint32_t IDESC_PV = ptx::idesc_f32acc(1, 1, false, true, 128, DV);
+
+  // Register split (setmaxnreg) of a 512-thread CTA launched with 128 registers per thread.
+  static constexpr int REG_SOFTMAX = 176, REG_CORR = 96, REG_MISC = 64;
+  static_assert(2 * 128 * REG_SOFTMAX + 128 * REG_CORR + 128 * REG_MISC <= 512 * 128,
+                "register split exceeds the launch allocation");
+};
+
+struct SchedSlot {
+  int32_t valid, b, h, t, q_start, lq, k_start, lk;
+};
+
+struct Ctx {
+  uint8_t* smem;
+  uint32_t sbase;
+  uint32_t tmem;
+  volatile int* abort_flag;
+  uint32_t* ws;
+  int bar_off;
+  __device__ __forceinline__ uint32_t bar(int i) const { return sbase + bar_off + 8u * (uint32_t)i; }
+};
+
+__device__ __forceinline__ void raise_error(const Ctx& c, int role, int id) {
+  if (atomicCAS(&c.ws[kWsErrorCode], 0u, (uint32_t)kDevErrTimeout) == 0u)
+    atomicExch(&c.ws[kWsErrorInfo], ((uint32_t)blockIdx.x << 16) | ((uint32_t)role << 8) | (uint32_t)id);
+  *c.abort_flag = 1;
+}
+
+// Warp-uniform bounded wait: every lane polls, the result is the same in all lanes.
+__device__ __forceinline__ bool wait_warp(const Ctx& c, int id, uint32_t parity, int role) {
+  const uint32_t bar = c.bar(id);
+  if (__all_sync(kFull, ptx::mbar_try_wait(bar, parity))) return true;
+  const uint64_t t0 = __shfl_sync(kFull, ptx::globaltimer(), 0);
+  for (uint32_t it = 1;; ++it) {
+    if (__all_sync(kFull, ptx::mbar_try_wait(bar, parity))) return true;
+    if ((it & 63u) == 0u) {
+      if (__any_sync(kFull, *c.abort_flag != 0)) return false;
+      const uint64_t now = __shfl_sync(kFull, ptx::globaltimer(), 0);
+      if (now - t0 > kTimeoutNs) {
+        if ((threadIdx.x & 31) == 0) raise_error(c, role, id);
+        __syncwarp();
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait of one thread that ignores the abort flag (drain paths).
+__device__ __forceinline__ bool wait_drain(const Ctx& c, int id, uint32_t parity) {
+  const uint32_t bar = c.bar(id);
+  const uint64_t t0 = ptx::globaltimer();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer() - t0 > kDrainTimeoutNs) return false;
+  }
+  return true;
+}
+
+// Ring position: stage index and phase parity.
+template <int N>
+struct Ring {
+  uint32_t idx = 0, phase = 0;
+  __device__ __forceinline__ void next() {
+    if (++idx == (uint32_t)N) {
+      idx = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+struct Geo {
+  int q0;      // first row (within its sequence) of Q tile 0
+  int n[2];    // K/V tiles each Q tile visits
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ Geo tile_geo(const SchedSlot& s) {
+  Geo g;
+  g.q0 = s.t * kRowsPerTile;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int kv_end = CAUSAL ? min(s.lk, g.q0 + kBlockM * (i + 1)) : s.lk;
+    g.n[i] = kv_end > 0 ? (kv_end + kBlockN - 1) / kBlockN : 0;
+  }
+  return g;
+}
+
+__device__ __forceinline__ SchedSlot read_slot(const Ctx& c, int slot, int off_sched) {
+  const volatile int32_t* p = reinterpret_cast<const volatile int32_t*>(c.smem + off_sched + 32 * slot);
+  SchedSlot s;
+  s.valid = p[0]; s.b = p[1]; s.h = p[2]; s.t = p[3];
+  s.q_start = p[4]; s.lq = p[5]; s.k_start = p[6]; s.lk = p[7];
+  return s;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Scheduler decode (warp 13, all lanes): work index -> work tile.
+struct Cursor {
+  int b = 0;
+  int64_t base = 0;
+};
+
+__device__ __forceinline__ SchedSlot decode_work(const Tc05Params& P, int64_t w, Cursor& cur) {
+  SchedSlot s;
+  s.valid = 0;
+  s.b = s.h = s.t = s.q_start = s.k_start = 0;
+  s.lq = P.seqlen_q;
+  s.lk = P.seqlen_k;
+  if (!P.packed) {
+    if (w < P.total_work) {
+      const WorkTile wt = decode_fixed(w, P.tiles_per_seq, P.heads_q, P.group);
+      s.valid = 1; s.b = wt.b; s.h = wt.h; s.t = wt.t;
+    }
+    return s;
+  }
+  const int lane = threadIdx.x & 31;
+  while (true) {
+    const int bb = cur.b + lane;
+    int64_t u = 0;
+    if (bb < P.batch) u = (int64_t)tiles_for(P.cu_q[bb + 1] - P.cu_q[bb], kRowsPerTile) * P.heads_q;
+    int64_t incl = u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t n = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += n;
+    }
+    const unsigned hit = __ballot_sync(kFull, bb < P.batch && w < cur.base + incl);
+    if (hit) {
+      const int L = __ffs(hit) - 1;
+      cur.base += __shfl_sync(kFull, incl - u, L);
+      cur.b += L;
+      const int b = cur.b;
+      const int qs = P.cu_q[b], qe = P.cu_q[b + 1], ks = P.cu_k[b], ke = P.cu_k[b + 1];
+      const WorkTile wt = decode_in_sequence(w - cur.base, b, tiles_for(qe - qs, kRowsPerTile), P.group);
+      s.valid = 1; s.b = b; s.h = wt.h; s.t = wt.t;
+      s.q_start = qs; s.lq = qe - qs; s.k_start = ks; s.lk = ke - ks;
+      return s;
+    }
+    if (cur.b + 32 >= P.batch) return s;
+    cur.base += __shfl_sync(kFull, incl, 31);
+    cur.b += 32;
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+template <class T, bool CAUSAL>
+__device__ void role_load_qk(const Tc05Params& P, const Ctx& c) {
+  const int lane = threadIdx.x & 31;
+  Ring<2> sched;
+  Ring<T::NK> kr;
+  uint32_t q_empty_phase = 0;
+  uint32_t k_fill_parity[T::NK];
+  bool k_used[T::NK];
+  bool q_used = false;
+#pragma unroll
+  for (int s = 0; s < T::NK; ++s) { k_fill_parity[s] = 0; k_used[s] = false; }
+  Cursor cur;
+  int64_t w = blockIdx.x;
+  bool aborted = false;
+  while (true) {
+    const SchedSlot s = decode_work(P, w, cur);
+    if (!wait_warp(c, BAR_SCHED_EMPTY + sched.idx, sched.phase ^ 1u, kRoleLoadQK)) { aborted = true; break; }
+    if (lane == 0) {
+      volatile int32_t* p = reinterpret_cast<volatile int32_t*>(c.smem + T::OFF_SCHED + 32 * sched.idx);
+      p[0] = s.valid; p[1] = s.b; p[2] = s.h; p[3] = s.t;
+      p[4] = s.q_start; p[5] = s.lq; p[6] = s.k_start; p[7] = s.lk;
+      ptx::mbar_arrive(c.bar(BAR_SCHED_FULL + sched.idx));
+    }
+    __syncwarp();
+    sched.next();
+    if (!s.valid) break;
+    const Geo g = tile_geo<CAUSAL>(s);
+    const int n1 = g.n[1];
+    if (n1 > 0) {
+      const int hk = s.h / P.group;
+      const int qb = P.packed ? 0 : s.b;
+      if (!wait_warp(c, BAR_Q_EMPTY, q_empty_phase ^ 1u, kRoleLoadQK)) { aborted = true; break; }
+      q_empty_phase ^= 1u;
+      if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const uint32_t bar = c.bar(BAR_Q_FULL + i);
+          const uint32_t dst = c.sbase + T::OFF_Q + i * T::Q_TILE_BYTES;
+          const int row = s.q_start + g.q0 + kBlockM * i;
+          ptx::mbar_expect_tx(bar, T::Q_TILE_BYTES);
+#pragma unroll
+          for (int ch = 0; ch < T::QK_CHUNKS; ++ch)
+            ptx::tma_load_4d(dst + ch * T::CHUNK_BYTES, &P.tm_q, bar, ch * T::QK_CHUNK_ELEMS, s.h, row, qb);
+          if (T::DR > 0)
+            ptx::tma_load_4d(dst + T::QK_CHUNKS * T::CHUNK_BYTES, &P.tm_qr, bar, 0, s.h, row, qb);
+        }
+      }
+      q_used = true;
+      for (int j = 0; j < n1; ++j) {
+        if (!wait_warp(c, T::BAR_K_EMPTY + kr.idx, kr.phase ^ 1u, kRoleLoadQK)) { aborted = true; break; }
+        if (lane == 0) {
+          const uint32_t bar = c.bar(T::BAR_K_FULL + kr.idx);
+          const uint32_t dst = c.sbase + T::OFF_K + kr.idx * T::K_STAGE_BYTES;
+          const int row = s.k_start + kBlockN * j;
+          ptx::mbar_expect_tx(bar, T::K_STAGE_BYTES);
+#pragma unroll
+          for (int ch = 0; ch < T::QK_CHUNKS; ++ch)
+            ptx::tma_load_4d(dst + ch * T::CHUNK_BYTES, &P.tm_k, bar, ch * T::QK_CHUNK_ELEMS, hk, row, qb);
+          if (T::DR > 0) ptx::tma_load_4d(dst + T::QK_CHUNKS * T::CHUNK_BYTES, &P.tm_kr, bar, 0, 0, row, qb);
+        }
+        k_fill_parity[kr.idx] = kr.phase;
+        k_used[kr.idx] = true;
+        kr.next();
+      }
+      if (aborted) break;
+    }
+    // next work index (dynamic)
+    int64_t nw = 0;
+    if (lane == 0) nw = (int64_t)gridDim.x + (int64_t)atomicAdd(&c.ws[kWsTileCounter], 1u);
+    w = __shfl_sync(kFull, nw, 0);
+  }
+  if (aborted && lane == 0) {
+    // Let every copy this warp issued land before the CTA exits.
+#pragma unroll
+    for (int s = 0; s < T::NK; ++s)
+      if (k_used[s]) wait_drain(c, T::BAR_K_FULL + s, k_fill_parity[s]);
+    if (q_used) {
+      wait_drain(c, BAR_Q_FULL + 0, (q_empty_phase ^ 1u));
+      wait_drain(c, BAR_Q_FULL + 1, (q_empty_phase ^ 1u));
+    }
+  }
+  __syncwarp();
+}
+
+template <class T, bool CAUSAL>
+__device__ void role_load_v(const Tc05Params& P, const Ctx& c) {
+  const int lane = threadIdx.x & 31;
+  Ring<2> sched;
+  Ring<T::NV> vr;
+  uint32_t v_fill_parity[T::NV];
+  bool v_used[T::NV];
+#pragma unroll
+  for (int s = 0; s < T::NV; ++s) { v_fill_parity[s] = 0; v_used[s] = false; }
+  bool aborted = false;
+  while (true) {
+    if (!wait_warp(c, BAR_SCHED_FULL + sched.idx, sched.phase, kRoleLoadV)) { aborted = true; break; }
+    const SchedSlot s = read_slot(c, sched.idx, T::OFF_SCHED);
+    if (lane == 0) ptx::mbar_arrive(c.bar(BAR_SCHED_EMPTY + sched.idx));
+    sched.next();
+    if (!s.valid) break;
+    const Geo g = tile_geo<CAUSAL>(s);
+    const int hk = s.h / P.group;
+    const int vb = P.packed ? 0 : s.b;
+    for (int j = 0; j < g.n[1]; ++j) {
+      if (!wait_warp(c, T::BAR_V_EMPTY + vr.idx, vr.phase ^ 1u, kRoleLoadV)) { aborted = true; break; }
+      if (lane == 0) {
+        const uint32_t bar = c.bar(T::BAR_V_FULL + vr.idx);
+        const uint32_t dst = c.sbase + T::OFF_V + vr.idx * T::V_STAGE_BYTES;
+        const int row = s.k_start + kBlockN * j;
+        ptx::mbar_expect_tx(bar, T::V_STAGE_BYTES);
+#pragma unroll
+        for (int ch = 0; ch < T::V_CHUNKS; ++ch)
+          ptx::tma_load_4d(dst + ch * T::CHUNK_BYTES, &P.tm_v, bar, ch * 64, hk, row, vb);
+      }
+      v_fill_parity[vr.idx] = vr.phase;
+      v_used[vr.idx] = true;
+      vr.next();
+    }
+    if (aborted) break;
+  }
+  if (aborted && lane == 0) {
+#pragma unroll
+    for (int s = 0; s < T::NV; ++s)
+      if (v_used[s]) wait_drain(c, T::BAR_V_FULL + s, v_fill_parity[s]);
+  }
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------------------------------------
+template <class T>
+__device__ __forceinline__ void issue_s(const Ctx& c, int i, uint32_t kstage) {
+  const uint32_t d = c.tmem + T::tm_s(i);
+  const uint32_t qa = ptx::opaque(c.sbase + T::OFF_Q + i * T::Q_TILE_BYTES);
+  const uint32_t ka = ptx::opaque(c.sbase + T::OFF_K + kstage * T::K_STAGE_BYTES);
+  if (T::FP8) {
+#pragma unroll
+    for (int kk = 0; kk < T::DQK / 32; ++kk)
+      ptx::mma_fp8_ss(d, ptx::sdesc_sw128(qa + kk * 32, 16, 1024), ptx::sdesc_sw128(ka + kk * 32, 16, 1024),
+                      T::IDESC_S, kk > 0);
+  } else {
+#pragma unroll
+    for (int kk = 0; kk < T::DQK / 16; ++kk) {
+      const uint32_t off = (kk >> 2) * T::CHUNK_BYTES + (kk & 3) * 32;
+      ptx::mma_bf16_ss(d, ptx::sdesc_sw128(qa + off, 16, 1024), ptx::sdesc_sw128(ka + off, 16, 1024), T::IDESC_S,
+                       kk > 0);
+    }
+#pragma unroll
+    for (int kk = 0; kk < T::DR / 16; ++kk) {
+      const uint32_t off = T::QK_CHUNKS * T::CHUNK_BYTES + kk * 32;
+      ptx::mma_bf16_ss(d, ptx::sdesc_sw128(qa + off, 16, 1024), ptx::sdesc_sw128(ka + off, 16, 1024), T::IDESC_S,
+                       1u);
+    }
+  }
+}
+
+template <class T>
+__device__ __forceinline__ void issue_pv(const Ctx& c, int i, uint32_t vstage, bool accumulate) {
+  const uint32_t d = c.tmem + T::tm_o(i);
+  const uint32_t a = c.tmem + T::tm_s(i);
+  const uint32_t va = ptx::opaque(c.sbase + T::OFF_V + vstage * T::V_STAGE_BYTES);
+#pragma unroll
+  for (int kk = 0; kk < kBlockN / 16; ++kk)
+    ptx::mma_bf16_ts(d, a + kk * 8, ptx::sdesc_sw128(va + kk * 2048, T::CHUNK_BYTES, 1024), T::IDESC_PV,
+                     (accumulate || kk > 0) ? 1u : 0u);
+}
+
+template <class T, bool CAUSAL>
+__device__ void role_mma(const Tc05Params& P, const Ctx& c) {
+  const bool leader = (threadIdx.x & 31) == 0;
+  Ring<2> sched;
+  Ring<T::NK> kr;   // stage of the next K tile to consume
+  Ring<T::NV> vr;   // stage of the next V tile to consume
+  uint32_t q_full_phase = 0;
+  uint32_t p_phase = 0, ocorr_phase = 0, ofree_phase = 0;   // bit i: Q tile i
+  bool aborted = false;
+#define AF_WAIT(id, par)                      \
+  if (!wait_warp(c, (id), (par), kRoleMma)) { \
+    aborted = true;                           \
+    break;                                    \
+  }
+  while (true) {
+    if (!wait_warp(c, BAR_SCHED_FULL + sched.idx, sched.phase, kRoleMma)) { aborted = true; break; }
+    const SchedSlot s = read_slot(c, sched.idx, T::OFF_SCHED);
+    if (leader) ptx::mbar_arrive(c.bar(BAR_SCHED_EMPTY + sched.idx));
+    sched.next();
+    if (!s.valid) break;
+    const Geo g = tile_geo<CAUSAL>(s);
+    const int n0 = g.n[0], n1 = g.n[1];
+    if (n1 == 0) {
+      // No keys: keep the per-tile O-free handshake in step with the epilogue.
+      AF_WAIT(BAR_O_FREE + 0, (ofree_phase & 1u) ^ 1u);
+      AF_WAIT(BAR_O_FREE + 1, ((ofree_phase >> 1) & 1u) ^ 1u);
+      ofree_phase ^= 3u;
+      continue;
+    }
+    // j = 0: S_0 of both Q tiles.
+    AF_WAIT(BAR_Q_FULL + 0, q_full_phase);
+    AF_WAIT(T::BAR_K_FULL + kr.idx, kr.phase);
+    ptx::tc_fence_after();
+    if (leader) {
+      issue_s<T>(c, 0, kr.idx);
+      ptx::mma_commit(c.bar(BAR_S_FULL + 0));
+    }
+    __syncwarp();
+    AF_WAIT(BAR_Q_FULL + 1, q_full_phase);
+    q_full_phase ^= 1u;
+    ptx::tc_fence_after();
+    if (leader) {
+      issue_s<T>(c, 1, kr.idx);
+      ptx::mma_commit(c.bar(BAR_S_FULL + 1));
+      ptx::mma_commit(c.bar(T::BAR_K_EMPTY + kr.idx));
+      if (n1 == 1) ptx::mma_commit(c.bar(BAR_Q_EMPTY));
+    }
+    __syncwarp();
+    kr.next();
+    for (int j = 1; j <= n1; ++j) {
+      const int jp = j - 1;
+      bool v_ready = false, k_ready = false;
+      if (jp < n0) {  // O_0 += P_0 V_{j-1}
+        AF_WAIT(BAR_P_FULL + 0, p_phase & 1u);
+        p_phase ^= 1u;
+        if (jp == 0) {
+          AF_WAIT(BAR_O_FREE + 0, (ofree_phase & 1u) ^ 1u);
+          ofree_phase ^= 1u;
+        } else {
+          AF_WAIT(BAR_O_CORR + 0, ocorr_phase & 1u);
+          ocorr_phase ^= 1u;
+        }
+        AF_WAIT(T::BAR_V_FULL + vr.idx, vr.phase);
+        v_ready = true;
+        ptx::tc_fence_after();
+        if (leader) {
+          issue_pv<T>(c, 0, vr.idx, jp > 0);
+          if (jp == n0 - 1) ptx::mma_commit(c.bar(BAR_O_FINAL + 0));
+        }
+        __syncwarp();
+      }
+      if (j < n0) {  // S_0 = Q_0 K_j^T
+        AF_WAIT(T::BAR_K_FULL + kr.idx, kr.phase);
+        k_ready = true;
+        ptx::tc_fence_after();
+        if (leader) {
+          issue_s<T>(c, 0, kr.idx);
+          ptx::mma_commit(c.bar(BAR_S_FULL + 0));
+        }
+        __syncwarp();
+      }
+      {  // O_1 += P_1 V_{j-1}
+        AF_WAIT(BAR_P_FULL + 1, (p_phase >> 1) & 1u);
+        p_phase ^= 2u;
+        if (jp == 0) {
+          AF_WAIT(BAR_O_FREE + 1, ((ofree_phase >> 1) & 1u) ^ 1u);
+          ofree_phase ^= 2u;
+        } else {
+          AF_WAIT(BAR_O_CORR + 1, (ocorr_phase >> 1) & 1u);
+          ocorr_phase ^= 2u;
+        }
+        if (!v_ready) AF_WAIT(T::BAR_V_FULL + vr.idx, vr.phase);
+        ptx::tc_fence_after();
+        if (leader) {
+          issue_pv<T>(c, 1, vr.idx, jp > 0);
+          ptx::mma_commit(c.bar(T::BAR_V_EMPTY + vr.idx));
+          if (jp == n1 - 1) ptx::mma_commit(c.bar(BAR_O_FINAL + 1));
+        }
+        __syncwarp();
+        vr.next();
+      }
+      if (j < n1) {  // S_1 = Q_1 K_j^T
+        if (!k_ready) AF_WAIT(T::BAR_K_FULL + kr.idx, kr.phase);
+        ptx::tc_fence_after();
+        if (leader) {
+          issue_s<T>(c, 1, kr.idx);
+          ptx::mma_commit(c.bar(BAR_S_FULL + 1));
+          ptx::mma_commit(c.bar(T::BAR_K_EMPTY + kr.idx));
+          if (j == n1 - 1) ptx::mma_commit(c.bar(BAR_Q_EMPTY));
+        }
+        __syncwarp();
+        kr.next();
+      }
+    }
+    if (aborted) break;
+  }
+#undef AF_WAIT
+  // Drain: the arrive of this commit follows every MMA and commit issued before it.
+  if (leader) {
+    ptx::mma_commit(c.bar(BAR_DRAIN));
+    wait_drain(c, BAR_DRAIN, 0);
+  }
+  (void)aborted;
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------------------------------------
+template <class T, bool CAUSAL>
+__device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
+  const int tid = threadIdx.x - 128 * i;          // row of the Q tile == TMEM lane
+  const uint32_t lane_base = (uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16;
+  const uint32_t tS = c.tmem + lane_base + T::tm_s(i);
+  float* alpha_sm = reinterpret_cast<float*>(c.smem + T::OFF_ALPHA) + i * kBlockM;
+  float* rcpl_sm = reinterpret_cast<float*>(c.smem + T::OFF_RCPL) + i * kBlockM;
+  float* ks_sm = reinterpret_cast<float*>(c.smem + T::OFF_KS) + i * 2 * kBlockN;
+  const int role = i == 0 ? kRoleSoftmax0 : kRoleSoftmax1;
+  Ring<2> sched;
+  uint32_t s_phase = 0, ks_phase = 0, stats_phase = 0;
+  while (true) {
+    if (!wait_warp(c, BAR_SCHED_FULL + sched.idx, sched.phase, role)) return;
+    const SchedSlot s = read_slot(c, sched.idx, T::OFF_SCHED);
+    ptx::mbar_arrive(c.bar(BAR_SCHED_EMPTY + sched.idx));
+    sched.next();
+    if (!s.valid) return;
+    const Geo g = tile_geo<CAUSAL>(s);
+    const int n = g.n[i];
+    const int qi = g.q0 + kBlockM * i + tid;     // row within the sequence
+    const bool row_valid = qi < s.lq;
+    const int lim = CAUSAL ? min(s.lk, qi + 1) : s.lk;   // keys visible to this row
+    const int first_row = g.q0 + kBlockM * i;
+    float c_row = P.scale_log2;
+    int64_t ks_base = 0;
+    if (T::FP8) {
+      const int hk = s.h / P.group;
+      float qs = 1.f;
+      if (row_valid)
+        qs = P.packed ? P.q_scale[(int64_t)s.h * P.total_q + s.q_start + qi]
+                      : P.q_scale[((int64_t)s.b * P.heads_q + s.h) * P.seqlen_q + qi];
+      c_row *= qs;
+      ks_base = P.packed ? (int64_t)hk * P.total_k + s.k_start : ((int64_t)s.b * P.heads_kv + hk) * P.seqlen_k;
+    }
+    float ks_next = 0.f;
+    if (T::FP8 && n > 0) ks_next = tid < s.lk ? __ldg(P.k_scale + ks_base + tid) : 0.f;
+    float m = -INFINITY, l = 0.f;
+    for (int j = 0; j < n; ++j) {
+      const int kb = kBlockN * j;
+      if (T::FP8) {
+        ks_sm[(j & 1) * kBlockN + tid] = ks_next;
+        ptx::mbar_arrive(c.bar(BAR_KS + i));
+        if (!wait_warp(c, BAR_KS + i, ks_phase, role)) return;
+        ks_phase ^= 1u;
+        if (j + 1 < n) ks_next = (kb + kBlockN + tid < s.lk) ? __ldg(P.k_scale + ks_base + kb + kBlockN + tid) : 0.f;
+      }
+      if (!wait_warp(c, BAR_S_FULL + i, s_phase, role)) return;
+      s_phase ^= 1u;
+      ptx::tc_fence_after();
+      float sv[128];
+      {
+        uint32_t r[32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          ptx::tmem_ld32(tS + 32 * q, r);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) sv[32 * q + e] = __uint_as_float(r[e]);
+        }
+      }
+      if (T::FP8) {
+        const float4* k4 = reinterpret_cast<const float4*>(ks_sm + (j & 1) * kBlockN);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float4 kv = k4[e];
+          sv[4 * e + 0] *= kv.x;
+          sv[4 * e + 1] *= kv.y;
+          sv[4 * e + 2] *= kv.z;
+          sv[4 * e + 3] *= kv.w;
+        }
+      }
+      const bool need_mask = (kb + kBlockN > s.lk) || (CAUSAL && kb + kBlockN - 1 > first_row);
+      if (need_mask) {
+        const int vis = lim - kb;
+#pragma unroll
+        for (int e = 0; e < 128; ++e)
+          if (e >= vis) sv[e] = -INFINITY;
+      }
+      float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
+#pragma unroll
+      for (int e = 4; e < 128; e += 4) {
+        mx0 = fmaxf(mx0, sv[e]);
+        mx1 = fmaxf(mx1, sv[e + 1]);
+        mx2 = fmaxf(mx2, sv[e + 2]);
+        mx3 = fmaxf(mx3, sv[e + 3]);
+      }
+      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c_row;
+      const float m_new = fmaxf(m, mx);
+      float m_use = m, alpha = 1.f;
+      if (j == 0) {
+        m_use = m_new;
+      } else if (m_new > m + 8.f) {
+        m_use = m_new;
+        alpha = ptx::ex2(m - m_new);
+      }
+      if (j > 0) {
+        alpha_sm[tid] = alpha;
+        ptx::mbar_arrive(c.bar(BAR_ALPHA + i));
+      }
+      const float neg = -m_use;
+      float s0 = 0.f, s1 = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int e = 0; e < 64; ++e) {
+        const float p0 = ptx::ex2(fmaf(sv[2 * e], c_row, neg));
+        const float p1 = ptx::ex2(fmaf(sv[2 * e + 1], c_row, neg));
+        s0 += p0;
+        s1 += p1;
+        pk[e] = ptx::pack_bf16(p0, p1);
+      }
+      l = l * alpha + (s0 + s1);
+      ptx::tmem_st32(tS, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+      ptx::tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(c.bar(BAR_P_FULL + i));
+      m = m_use;
+    }
+    // Row statistics: LSE (natural log) here, 1/l to the epilogue.
+    if (row_valid && P.lse != nullptr) {
+      const float lse = l > 0.f ? (m + ptx::lg2(l)) * 0.69314718055994531f : -INFINITY;
+      if (P.packed) P.lse[(int64_t)s.h * P.total_q + s.q_start + qi] = lse;
+      else P.lse[((int64_t)s.b * P.heads_q + s.h) * P.seqlen_q + qi] = lse;
+    }
+    if (!wait_warp(c, BAR_STATS_FREE + i, stats_phase ^ 1u, role)) return;
+    stats_phase ^= 1u;
+    rcpl_sm[tid] = l > 0.f ? 1.f / l : 0.f;
+    ptx::mbar_arrive(c.bar(BAR_ALPHA + i));
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+template <class T>
+__device__ __forceinline__ void store_row_chunk(uint16_t* dst, const uint32_t (&r)[32], float scale) {
+  uint32_t pk[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e)
+    pk[e] = ptx::pack_bf16(__uint_as_float(r[2 * e]) * scale, __uint_as_float(r[2 * e + 1]) * scale);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) d[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+}
+
+template <class T, bool CAUSAL>
+__device__ void role_correction(const Tc05Params& P, const Ctx& c) {
+  const int tid = threadIdx.x - 256;
+  const uint32_t lane_base = (uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16;
+  const float* alpha_sm = reinterpret_cast<const float*>(c.smem + T::OFF_ALPHA);
+  const float* rcpl_sm = reinterpret_cast<const float*>(c.smem + T::OFF_RCPL);
+  Ring<2> sched;
+  uint32_t alpha_phase[2] = {0, 0}, ofinal_phase[2] = {0, 0};
+  while (true) {
+    if (!wait_warp(c, BAR_SCHED_FULL + sched.idx, sched.phase, kRoleCorrection)) return;
+    const SchedSlot s = read_slot(c, sched.idx, T::OFF_SCHED);
+    ptx::mbar_arrive(c.bar(BAR_SCHED_EMPTY + sched.idx));
+    sched.next();
+    if (!s.valid) return;
+    const Geo g = tile_geo<CAUSAL>(s);
+
+    auto correct = [&](int i) -> bool {
+      if (!wait_warp(c, BAR_ALPHA + i, alpha_phase[i], kRoleCorrection)) return false;
+      alpha_phase[i] ^= 1u;
+      const float a = alpha_sm[i * kBlockM + tid];
+      if (__any_sync(kFull, a != 1.f)) {
+        ptx::tc_fence_after();
+        const uint32_t tO = c.tmem + lane_base + T::tm_o(i);
+#pragma unroll
+        for (int q = 0; q < T::DV / 32; ++q) {
+          uint32_t r[32];
+          ptx::tmem_ld32(tO + 32 * q, r);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * a);
+          ptx::tmem_st32(tO + 32 * q, r);
+        }
+        ptx::tmem_wait_st();
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(c.bar(BAR_O_CORR + i));
+      return true;
+    };
+
+    auto epilogue = [&](int i) -> bool {
+      if (!wait_warp(c, BAR_ALPHA + i, alpha_phase[i], kRoleCorrection)) return false;
+      alpha_phase[i] ^= 1u;
+      const float rl = rcpl_sm[i * kBlockM + tid];
+      ptx::mbar_arrive(c.bar(BAR_STATS_FREE + i));
+      const int qi = g.q0 + kBlockM * i + tid;
+      const bool row_valid = qi < s.lq;
+      uint16_t* orow = P.o + (int64_t)s.b * P.o_stride_b + (int64_t)(s.q_start + qi) * P.o_stride_t +
+                       (int64_t)s.h * P.o_stride_h;
+      if (g.n[i] > 0) {
+        if (!wait_warp(c, BAR_O_FINAL + i, ofinal_phase[i], kRoleCorrection)) return false;
+        ofinal_phase[i] ^= 1u;
+        ptx::tc_fence_after();
+        const uint32_t tO = c.tmem + lane_base + T::tm_o(i);
+#pragma unroll
+        for (int q = 0; q < T::DV / 32; ++q) {
+          uint32_t r[32];
+          ptx::tmem_ld32(tO + 32 * q, r);
+          ptx::tmem_wait_ld();
+          if (row_valid) store_row_chunk<T>(orow + 32 * q, r, rl);
+        }
+      } else if (row_valid) {
+        uint4* d = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+        for (int e = 0; e < T::DV / 8; ++e) d[e] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(c.bar(BAR_O_FREE + i));
+      return true;
+    };
+
+    const int n1 = g.n[1];
+    if (n1 == 0) {
+      if (!epilogue(0) || !epilogue(1)) return;
+      continue;
+    }
+    for (int jj = 1; jj <= n1; ++jj) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        if (jj < g.n[i]) {
+          if (!correct(i)) return;
+        } else if (jj == g.n[i]) {
+          if (!epilogue(i)) return;
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <class T, bool CAUSAL>
+__global__ void __launch_bounds__(512, 1) fa_tc05_kernel(const __grid_constant__ Tc05Params P) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  Ctx c;
+  c.smem = smem;
+  c.sbase = ptx::smem_u32(smem);
+  c.ws = P.ws;
+  c.abort_flag = reinterpret_cast<volatile int*>(smem + T::OFF_ABORT);
+  c.bar_off = T::OFF_BAR;
+  if (c.sbase & 1023u) {  // the swizzled tiles need a 1024-byte aligned base
+    if (threadIdx.x == 0) atomicCAS(&P.ws[kWsErrorCode], 0u, 2u);
+    return;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(c.bar(BAR_Q_FULL + i), 1);
+      ptx::mbar_init(c.bar(BAR_S_FULL + i), 1);
+      ptx::mbar_init(c.bar(BAR_P_FULL + i), 128);
+      ptx::mbar_init(c.bar(BAR_ALPHA + i), 128);
+      ptx::mbar_init(c.bar(BAR_O_CORR + i), 128);
+      ptx::mbar_init(c.bar(BAR_O_FINAL + i), 1);
+      ptx::mbar_init(c.bar(BAR_O_FREE + i), 128);
+      ptx::mbar_init(c.bar(BAR_STATS_FREE + i), 128);
+      ptx::mbar_init(c.bar(BAR_KS + i), 128);
+      ptx::mbar_init(c.bar(BAR_SCHED_FULL + i), 1);
+      ptx::mbar_init(c.bar(BAR_SCHED_EMPTY + i), kSchedConsumers);
+    }
+    ptx::mbar_init(c.bar(BAR_Q_EMPTY), 1);
+    ptx::mbar_init(c.bar(BAR_DRAIN), 1);
+#pragma unroll
+    for (int s = 0; s < T::NK; ++s) {
+      ptx::mbar_init(c.bar(T::BAR_K_FULL + s), 1);
+      ptx::mbar_init(c.bar(T::BAR_K_EMPTY + s), 1);
+    }
+#pragma unroll
+    for (int s = 0; s < T::NV; ++s) {
+      ptx::mbar_init(c.bar(T::BAR_V_FULL + s), 1);
+      ptx::mbar_init(c.bar(T::BAR_V_EMPTY + s), 1);
+    }
+    *c.abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 12) {
+    ptx::tmem_alloc(c.sbase + T::OFF_TMEM_SLOT, T::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  if (warp == 13 && lane == 0) {
+    ptx::prefetch_tmap(&P.tm_q);
+    ptx::prefetch_tmap(&P.tm_k);
+    ptx::prefetch_tmap(&P.tm_v);
+    if (T::DR > 0) {
+      ptx::prefetch_tmap(&P.tm_qr);
+      ptx::prefetch_tmap(&P.tm_kr);
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  c.tmem = *reinterpret_cast<volatile uint32_t*>(smem + T::OFF_TMEM_SLOT);
+
+  const int wg = warp >> 2;
+  if (wg < 2) {
+    setmaxnreg_inc<T::REG_SOFTMAX>();
+    role_softmax<T, CAUSAL>(P, c, wg);
+  } else if (wg == 2) {
+    setmaxnreg_dec<T::REG_CORR>();
+    role_correction<T, CAUSAL>(P, c);
+  } else {
+    setmaxnreg_dec<T::REG_MISC>();
+    if (warp == 12) role_mma<T, CAUSAL>(P, c);
+    else if (warp == 13) role_load_qk<T, CAUSAL>(P, c);
+    else if (warp == 14) role_load_v<T, CAUSAL>(P, c);
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 12) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(c.tmem, T::TMEM_COLS);
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(&P.ws[kWsDoneCounter], 1u) == gridDim.x - 1) {
+      atomicExch(&P.ws[kWsTileCounter], 0u);
+      atomicExch(&P.ws[kWsDoneCounter], 0u);
+      __threadfence();
+    }
+  }
+}
+
+template <class T>
+cudaError_t tc05_launch_t(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream) {
+  auto kern = causal ? fa_tc05_kernel<T, true> : fa_tc05_kernel<T, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, 512, T::SMEM_BYTES, stream>>>(prm);
+  return cudaGetLastError();
+}
+
+template <class T>
+Tc05Config tc05_config_t() {
+  Tc05Config c;
+  c.smem_bytes = T::SMEM_BYTES;
+  c.k_stages = T::NK;
+  c.v_stages = T::NV;
+  c.threads = 512;
+  c.tmem_cols = (int)T::TMEM_COLS;
+  return c;
+}
+
+using TraitsD64 = Tc05Traits<64, 0, 64, false>;
+using TraitsD128 = Tc05Traits<128, 0, 128, false>;
+using TraitsD128R64 = Tc05Traits<128, 64, 128, false>;
+using TraitsFp8D128 = Tc05Traits<128, 0, 128, true>;
+
+cudaError_t tc05_launch_d64(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
+cudaError_t tc05_launch_d128(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
+cudaError_t tc05_launch_d128r64(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
+cudaError_t tc05_launch_fp8d128(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
+
+}  // namespace af

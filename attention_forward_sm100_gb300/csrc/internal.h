@@ -1,0 +1,78 @@
+// Declarations shared by the host API and the kernel translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/attn_fwd.h"
+
+namespace af {
+
+constexpr int kRowsPerTile = 256;   // query rows per work tile of the tcgen05 kernel
+constexpr int kBlockM = 128;        // query rows per MMA tile (one TMEM lane per row)
+constexpr int kBlockN = 128;        // keys per K/V tile
+
+// Workspace words (uint32 each).
+enum WorkspaceWord : int {
+  kWsTileCounter = 0,   // next dynamic work index minus gridDim.x
+  kWsDoneCounter = 1,   // CTAs finished (the last one resets both counters)
+  kWsErrorCode = 2,     // 0 or a device error code
+  kWsErrorInfo = 3,     // block, role and barrier of the first error
+  kWsWords = 4
+};
+
+// Device error codes recorded in kWsErrorCode.
+enum DeviceError : uint32_t {
+  kDevErrNone = 0,
+  kDevErrTimeout = 1,
+};
+
+// Everything the tcgen05 kernel needs, passed as one __grid_constant__ struct.
+struct Tc05Params {
+  CUtensorMap tm_q;        // Q (nope part): box {64 or 128 elements, 1, 128, 1}
+  CUtensorMap tm_k;        // K (nope part)
+  CUtensorMap tm_v;        // V: box {64, 1, 128, 1}
+  CUtensorMap tm_qr;       // Q rope part (rope only)
+  CUtensorMap tm_kr;       // K rope part (rope only): box {64, 1, 128, 1}
+  const float* q_scale;    // fp8 only
+  const float* k_scale;
+  const int32_t* cu_q;     // packed only
+  const int32_t* cu_k;
+  uint16_t* o;             // output rows (bf16 bits)
+  float* lse;
+  uint32_t* ws;            // workspace words
+  int64_t o_stride_b, o_stride_t, o_stride_h;  // elements
+  int32_t batch, seqlen_q, seqlen_k, heads_q, heads_kv, group;
+  int32_t tiles_per_seq;   // fixed length: ceil(Sq / kRowsPerTile)
+  int64_t total_work;      // fixed length: exact number of work tiles
+  int32_t packed;
+  int32_t total_q;         // packed: rows of q (LSE and q_scale layout [Hq, Tq])
+  int32_t total_k;         // packed: rows of k (k_scale layout [Hkv, Tk])
+  float scale_log2;        // softmax_scale * log2(e)
+};
+
+// Kernel variants of the tcgen05 path.
+enum Tc05Variant : int {
+  kVarD64 = 0,        // bf16, Dqk = Dv = 64
+  kVarD128 = 1,       // bf16, Dqk = Dv = 128
+  kVarD128Rope64 = 2, // bf16, Dqk = 128 + rope 64, Dv = 128
+  kVarFp8D128 = 3,    // fp8 e4m3 Q/K, Dqk = Dv = 128
+  kVarCount = 4
+};
+
+struct Tc05Config {
+  int smem_bytes;
+  int k_stages;
+  int v_stages;
+  int threads;
+  int tmem_cols;
+};
+
+// Static configuration of a variant (host).
+Tc05Config tc05_config(int variant);
+// Launch of one variant (defined in the per-variant translation units).
+cudaError_t tc05_launch(int variant, bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
+// Launch of the plain CUDA-core kernel.
+cudaError_t simple_launch(const attn_fwd_params& p, cudaStream_t stream);
+
+}  // namespace af

@@ -1,0 +1,25 @@
+// Variant table of the tcgen05 kernel: static configuration and launch.
+#include "fa_tc05.cuh"
+
+namespace af {
+
+Tc05Config tc05_config(int variant) {
+  switch (variant) {
+    case kVarD64: return tc05_config_t<TraitsD64>();
+    case kVarD128: return tc05_config_t<TraitsD128>();
+    case kVarD128Rope64: return tc05_config_t<TraitsD128R64>();
+    default: return tc05_config_t<TraitsFp8D128>();
+  }
+}
+
+cudaError_t tc05_launch(int variant, bool causal, const Tc05Params& prm, int grid, cudaStream_t stream) {
+  switch (variant) {
+    case kVarD64: return tc05_launch_d64(causal, prm, grid, stream);
+    case kVarD128: return tc05_launch_d128(causal, prm, grid, stream);
+    case kVarD128Rope64: return tc05_launch_d128r64(causal, prm, grid, stream);
+    case kVarFp8D128: return tc05_launch_fp8d128(causal, prm, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace af

@@ -1,0 +1,355 @@
+"""Throughput of the fused attention forward on GB300.
+
+One step = one attn_fwd call (the whole hot path: scheduling, TMA loads,
+QK^T, softmax, correction, PV and the epilogue) over the chosen workload,
+inputs resident in HBM. Prints one JSON line on rank 0.
+
+  python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl ours|reference]
+
+Multi-GPU (torchrun): every rank runs an independent replica of the workload
+(weak scaling, no collective on the data path); value = FLOPs of all ranks /
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "mha_b4_h16_s4096_d128_causal"
+METRIC = "attention fwd TFLOP/s at 1 GB300 and % of dense tensor peak (BF16/FP8)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 126 * 1024 * 1024
+# DRAM bytes per launch of the tcgen05 kernel on the default workload, from
+# the ncu capture summarised in profiles/ (None until captured for the
+# current kernel).
+TRAFFIC_BYTES = None
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def peak_tflops(spec, peaks):
+    """Dense tensor peak for the workload's MMA mix (bf16 burst; FP8 QK^T
+    counted at 2x the bf16 rate, i.e. half the FLOPs at 2x, blended)."""
+    bf16 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    if spec.qk_dtype == "fp8":
+        return 2.0 / (1.0 / (2.0 * bf16) + 1.0 / bf16)
+    return bf16
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.strip().split(",") for r in self.file.read().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower() in ("active", "1"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(spec, inputs, seconds):
+    """The fp64 oracle timed on the host cores over whole (sequence, head)
+    problems of the workload until `seconds` have passed; TFLOP/s of the
+    visible pairs processed."""
+    import numpy as np
+
+    import oracle
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from helpers import f64
+
+    cores = len(os.sched_getaffinity(0))
+    lq, lk = spec.seq_lengths()
+    q, k, v = f64(inputs["q"]), f64(inputs["k"]), f64(inputs["v"])
+    qr, kr = f64(inputs.get("q_rope")), f64(inputs.get("k_rope"))
+    qs, ks = f64(inputs.get("q_scale")), f64(inputs.get("k_scale"))
+    cu_q = inputs.get("cu_seqlens_q")
+    cu_k = inputs.get("cu_seqlens_k")
+    g = spec.heads_q // spec.heads_kv
+    done_flops, heads = 0, 0
+    t0 = time.perf_counter()
+    order = [(b, h) for h in range(spec.heads_q) for b in range(spec.batch)]
+    for b, h in order:
+        hk = h // g
+        if spec.varlen:
+            a, e = int(cu_q[b]), int(cu_q[b + 1])
+            c, f = int(cu_k[b]), int(cu_k[b + 1])
+            args = (q[a:e, h], k[c:f, hk], v[c:f, hk], spec.softmax_scale, spec.causal,
+                    None if qr is None else qr[a:e, h], None if kr is None else kr[c:f],
+                    None if qs is None else qs[h, a:e], None if ks is None else ks[hk, c:f])
+        else:
+            args = (q[b, :, h], k[b, :, hk], v[b, :, hk], spec.softmax_scale, spec.causal,
+                    None if qr is None else qr[b, :, h], None if kr is None else kr[b],
+                    None if qs is None else qs[b, h], None if ks is None else ks[b, hk])
+        oracle.attention_head(*args)
+        n, m = lq[b], lk[b]
+        pairs = (min(n, m) * (min(n, m) + 1) // 2 + max(0, n - m) * m) if spec.causal else n * m
+        done_flops += 2 * (spec.d_qk + spec.rope + spec.d_v) * pairs
+        heads += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    del np
+    return {"value": done_flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{heads} whole (sequence, head) problems of {spec.batch * spec.heads_q}, "
+                      f"fp64 numpy, {dt:.1f} s"}
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def run_reference(args, spec, world, rank):
+    """Reference arm: the CPU oracle as it stands, one bounded sample of the
+    workload per step."""
+    if rank != 0:
+        return
+    from attention_forward_sm100_gb300 import workloads as W
+    inputs = W.make_inputs(spec)
+    per_step = max(1.0, min(20.0, 100.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_baseline(spec, inputs, per_step / 4)
+    vals = []
+    last = None
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        last = cpu_baseline(spec, inputs, per_step)
+        vals.append(last["value"])
+    wall = time.perf_counter() - t0
+    value = statistics.mean(vals)
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": wall * 1e3 / max(1, args.steps), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": args.workload, "sample": last["sample"] if last else None},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": last["cores"], "kind": "oracle",
+                             "sample": last["sample"]},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    from attention_forward_sm100_gb300 import workloads as W
+    spec = W.WORKLOADS[args.workload]
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, spec, world, rank)
+        return
+
+    import torch
+
+    import attention_forward_sm100_gb300 as pkg
+    if args.warmup < 3:
+        args.warmup = 3
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pkg.lib()
+    inputs = W.make_inputs(spec)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inputs.items()}
+    lq, lk = spec.seq_lengths()
+    out = torch.empty(d["q"].shape[:-1] + (spec.d_v,), dtype=torch.bfloat16, device=dev)
+    if spec.varlen:
+        lse = torch.empty((spec.heads_q, d["q"].shape[0]), dtype=torch.float32, device=dev)
+    else:
+        lse = torch.empty((spec.batch, spec.heads_q, spec.seqlen_q), dtype=torch.float32, device=dev)
+    kw = dict(causal=spec.causal, softmax_scale=spec.softmax_scale, q_rope=d.get("q_rope"), k_rope=d.get("k_rope"),
+              q_scale=d.get("q_scale"), k_scale=d.get("k_scale"), cu_seqlens_q=d.get("cu_seqlens_q"),
+              cu_seqlens_k=d.get("cu_seqlens_k"), max_seqlen_q=max(lq), max_seqlen_k=max(lk), out=out, lse=lse)
+    in_bytes = sum(t.numel() * t.element_size() for t in d.values() if isinstance(t, torch.Tensor))
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        pkg.forward(d["q"], d["k"], d["v"], stream=stream, **kw)
+
+    for _ in range(args.warmup):
+        step()
+    pkg.check(device=dev)
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for i in range(args.steps):
+        step()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    pkg.check(device=dev)
+    per_launch = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    total_ms = max_over_ranks(total_ms, world, dev)
+    ms = total_ms / args.steps
+    flops = spec.flops()
+    value = flops * world / (ms * 1e-3) / 1e12
+    kernel_ms = statistics.mean(per_launch)
+    achieved = flops / (kernel_ms * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    peak = peak_tflops(spec, peaks)
+
+    e2e = None
+    if not args.no_e2e:
+        hq = inputs["q"].pin_memory()
+        hk = inputs["k"].pin_memory()
+        hv = inputs["v"].pin_memory()
+        extra = {n: inputs[n].pin_memory() for n in ("q_rope", "k_rope", "q_scale", "k_scale")
+                 if inputs.get(n) is not None}
+        ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in [hq, hk, hv] + list(extra.values()))
+        d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+
+        def e2e_step():
+            d["q"].copy_(hq, non_blocking=True)
+            d["k"].copy_(hk, non_blocking=True)
+            d["v"].copy_(hv, non_blocking=True)
+            for n, t in extra.items():
+                d[n].copy_(t, non_blocking=True)
+            step()
+            ho.copy_(out, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = max(3, min(args.steps, 10))
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world, dev)
+        e2e = {"value": flops * world / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+
+    cpu = None
+    if rank == 0 and world >= 1 and not args.no_cpu_baseline and args.gpus == 1:
+        cpu = cpu_baseline(spec, inputs, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp8+bf16" if spec.qk_dtype == "fp8" else "bf16",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "batch": spec.batch, "heads_q": spec.heads_q,
+                       "heads_kv": spec.heads_kv, "seqlen": spec.seqlen_q, "head_dim_qk": spec.d_qk + spec.rope,
+                       "head_dim_v": spec.d_v, "causal": spec.causal, "flops_per_step": flops,
+                       "l2": "inputs larger than L2" if in_bytes > L2_BYTES else "inputs fit in L2 (no flush)",
+                       "parallelism": f"replicas x{world}"},
+            "pct_of_peak": 100.0 * value / world / peak,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "peak_source": f"bf16 burst, {peak_src}",
+                         "traffic": TRAFFIC_BYTES},
+            "kernel_ms": kernel_ms,
+            "clocks": clk,
+            "gpu_launches": args.steps,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,168 @@
+/*
+ * attn_fwd.h - C ABI of the GB300 (sm_103a) fused attention forward library.
+ *
+ * Operation (the forward pass of the flash-attention kernel whose shared-memory
+ * layout the "SM100AttentionSMem" page documents; the rope sub-depth and the
+ * per-token Q/K scale are the optional parts of that page's Parameters
+ * section; the persistent work loop follows the "MHATileScheduler" page and
+ * the staged K/V loads the "TMAProducerPipeline" page):
+ *
+ *   for each sequence b, query head h, query row i:
+ *     hk    = h / (Hq / Hkv)                        consecutive query heads share a KV head
+ *     J_i   = { j < Sk_b : !causal || j <= i }      causal mask is top-left aligned
+ *     s_ij  = scale * (q_i . k_j + q_rope_i . k_rope_j)            bf16 Q/K (rope optional)
+ *     s_ij  = scale * q_scale_i * k_scale_j * (Q8_i . K8_j)         fp8 e4m3 Q/K
+ *     LSE_i = ln sum_{j in J_i} exp(s_ij)                           natural log
+ *     O_i   = sum_{j in J_i} exp(s_ij - LSE_i) * v_j                bf16, rounded once
+ *   Rows with an empty J_i get O_i = 0 and LSE_i = -inf.
+ *
+ * Conventions
+ *   - Every pointer in attn_fwd_params is a DEVICE pointer owned by the caller.
+ *     The library allocates no memory and keeps no mutable global state.
+ *   - attn_fwd() validates, encodes TMA descriptors on the host and enqueues
+ *     one kernel on `stream`; it returns without synchronising. Invalid
+ *     arguments are reported before anything is enqueued and no memory is
+ *     touched. No C++ exception crosses this boundary.
+ *   - Kernel-side failures (a bounded wait that ran out) are recorded in the
+ *     workspace and reported by attn_fwd_check().
+ */
+#ifndef ATTN_FWD_H
+#define ATTN_FWD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st *attn_stream_t;
+
+typedef enum attn_dtype {
+  ATTN_DTYPE_BF16 = 0,      /* Q and K bf16 */
+  ATTN_DTYPE_FP8_E4M3 = 1   /* Q and K float8_e4m3fn with per-token fp32 scales */
+} attn_dtype;
+
+typedef enum attn_status {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,     /* malformed arguments (null, misaligned, inconsistent sizes) */
+  ATTN_ERR_UNSUPPORTED = 2,     /* well-formed but not handled (head dims, dtype mix) */
+  ATTN_ERR_CUDA = 3,            /* a CUDA runtime/driver call failed */
+  ATTN_ERR_DEVICE_TIMEOUT = 4   /* a kernel wait ran out of time (see attn_fwd_check) */
+} attn_status;
+
+typedef enum attn_backend {
+  ATTN_BACKEND_TCGEN05 = 0,     /* persistent warp-specialised tcgen05/TMA kernel */
+  ATTN_BACKEND_SIMPLE = 1       /* plain fp32 CUDA-core kernel, for cross-checking only */
+} attn_backend;
+
+/* Bytes of workspace attn_fwd needs; the workspace holds the persistent
+ * scheduler's work counter and the device error record. */
+#define ATTN_FWD_WORKSPACE_BYTES 256
+
+typedef struct attn_fwd_params {
+  /* ---- tensors (device pointers, caller-owned) ------------------------- */
+  const void *q;        /* fixed [B,Sq,Hq,Dqk] / packed [Tq,Hq,Dqk]; bf16 or fp8 (qk_dtype) */
+  const void *k;        /* fixed [B,Sk,Hkv,Dqk] / packed [Tk,Hkv,Dqk]; same type as q */
+  const void *v;        /* fixed [B,Sk,Hkv,Dv] / packed [Tk,Hkv,Dv]; bf16 */
+  const void *q_rope;   /* rope_depth > 0 only: [B,Sq,Hq,R] / [Tq,Hq,R]; bf16 */
+  const void *k_rope;   /* rope_depth > 0 only: [B,Sk,R] / [Tk,R]; bf16, shared by all heads */
+  const float *q_scale; /* fp8 only: [B,Hq,Sq] / [Hq,Tq], contiguous fp32 */
+  const float *k_scale; /* fp8 only: [B,Hkv,Sk] / [Hkv,Tk], contiguous fp32 */
+  const int32_t *cu_seqlens_q; /* packed only: [B+1] prefix offsets of the query rows */
+  const int32_t *cu_seqlens_k; /* packed only: [B+1] prefix offsets of the key rows */
+  void *o;              /* fixed [B,Sq,Hq,Dv] / packed [Tq,Hq,Dv]; bf16, written */
+  float *lse;           /* [B,Hq,Sq] / [Hq,Tq] contiguous fp32, written; may be NULL */
+  void *workspace;      /* >= ATTN_FWD_WORKSPACE_BYTES device bytes, 256-byte aligned,
+                           zero-filled once before its first use; every call leaves it
+                           zeroed again. Calls that share a workspace must not overlap. */
+  size_t workspace_bytes;
+
+  /* ---- sizes ------------------------------------------------------------ */
+  int32_t batch;        /* B, number of sequences */
+  int32_t seqlen_q;     /* fixed: Sq; packed: an upper bound of every query length */
+  int32_t seqlen_k;     /* fixed: Sk; packed: an upper bound of every key length */
+  int32_t total_q;      /* packed only: Tq (rows of q and o) */
+  int32_t total_k;      /* packed only: Tk (rows of k and v) */
+  int32_t num_heads_q;  /* Hq */
+  int32_t num_heads_kv; /* Hkv, divides Hq */
+  int32_t head_dim_qk;  /* Dqk, depth of q and k without the rope part */
+  int32_t head_dim_v;   /* Dv */
+  int32_t rope_depth;   /* R, 0 or 64 */
+  int32_t causal;       /* non-zero: query i sees keys 0..i of its sequence */
+  float softmax_scale;  /* scale of the scores; > 0 */
+  int32_t qk_dtype;     /* attn_dtype */
+  int32_t backend;      /* attn_backend */
+
+  /* ---- element strides: [0] batch (unused when packed), [1] token, [2] head.
+   *      The innermost dimension is contiguous. --------------------------- */
+  int64_t q_stride[3];
+  int64_t k_stride[3];
+  int64_t v_stride[3];
+  int64_t o_stride[3];
+  int64_t q_rope_stride[3];
+  int64_t k_rope_stride[2]; /* [0] batch, [1] token */
+} attn_fwd_params;
+
+/* Query results of attn_fwd_plan (host only; no GPU needed). */
+typedef struct attn_fwd_plan_info {
+  int32_t backend;          /* kernel that attn_fwd would launch */
+  int32_t rows_per_tile;    /* query rows per work tile */
+  int64_t work_tiles;       /* fixed: exact count; packed: upper bound B*Hq*ceil(Sq/rows) */
+  int32_t grid;             /* CTAs launched (persistent: min(SMs, work_tiles)) */
+  int32_t block;            /* threads per CTA */
+  int32_t smem_bytes;       /* dynamic shared memory per CTA */
+  int32_t k_stages;         /* depth of the K ring */
+  int32_t v_stages;         /* depth of the V ring */
+  int32_t tmem_columns;     /* tensor-memory columns allocated per CTA */
+} attn_fwd_plan_info;
+
+/* One work tile as the persistent scheduler hands it out. */
+typedef struct attn_work_tile {
+  int32_t batch;            /* sequence b */
+  int32_t head;             /* query head h */
+  int32_t tile;             /* query tile t: rows [t*rows_per_tile, (t+1)*rows_per_tile) */
+} attn_work_tile;
+
+/* Fills `p` with zeros and the defaults (bf16, tcgen05 backend). */
+void attn_fwd_params_init(attn_fwd_params *p);
+
+/* sizeof(attn_fwd_params) as compiled into the library (binding check). */
+size_t attn_fwd_params_size(void);
+
+/* Workspace bytes needed for `p` (currently ATTN_FWD_WORKSPACE_BYTES). */
+size_t attn_fwd_workspace_bytes(const attn_fwd_params *p);
+
+/* Validates `p` and enqueues the forward on `stream`. Asynchronous. Errors:
+ * INVALID_ARG / UNSUPPORTED before launch; CUDA if the launch failed. */
+attn_status attn_fwd(const attn_fwd_params *p, attn_stream_t stream);
+
+/* Synchronises `stream`, reads and clears the device error record of
+ * `workspace`. Returns DEVICE_TIMEOUT if a kernel wait ran out, CUDA for a
+ * pending CUDA error, else OK. */
+attn_status attn_fwd_check(void *workspace, attn_stream_t stream);
+
+/* Validates `p` and reports the launch plan without touching the GPU,
+ * except for reading the SM count of the current device when one exists
+ * (148 SMs are assumed otherwise). */
+attn_status attn_fwd_plan(const attn_fwd_params *p, attn_fwd_plan_info *out);
+
+/* Host copy of the persistent scheduler's order: writes up to `cap` work
+ * tiles in the order the kernel hands them out and returns how many there
+ * are in total. `host_cu_seqlens_q` is a HOST array of B+1 offsets, or NULL
+ * for fixed length. Used to test the schedule on a CPU. */
+int64_t attn_fwd_schedule(const attn_fwd_params *p, const int32_t *host_cu_seqlens_q,
+                          attn_work_tile *out, int64_t cap);
+
+/* Static description of a status code. */
+const char *attn_status_string(attn_status s);
+
+/* Detail of the last error returned to the calling thread (empty if none). */
+const char *attn_fwd_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_FWD_H */

@@ -68,3 +68,40 @@ def assert_within(err, dtype):
     tol = TOL[dtype]
     for key, bound in tol.items():
         assert err[key] <= bound, f"{key}={err[key]:.3e} exceeds {bound:.1e} ({err})"
+
+
+def run_lib(inputs, backend="tcgen05", device="cuda"):
+    """Runs the library on a workload input dict; returns (O, LSE) as CPU tensors."""
+    import attention_forward_sm100_gb300 as pkg
+    spec = inputs["spec"]
+    dev = torch.device(device)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inputs.items()}
+    lq, lk = spec.seq_lengths()
+    o, lse = pkg.forward(d["q"], d["k"], d["v"], causal=spec.causal, softmax_scale=spec.softmax_scale,
+                         q_rope=d.get("q_rope"), k_rope=d.get("k_rope"), q_scale=d.get("q_scale"),
+                         k_scale=d.get("k_scale"), cu_seqlens_q=d.get("cu_seqlens_q"),
+                         cu_seqlens_k=d.get("cu_seqlens_k"), max_seqlen_q=max(lq + [0]),
+                         max_seqlen_k=max(lk + [0]), backend=backend)
+    pkg.check(device=dev)
+    return o.cpu(), lse.cpu()
+
+
+def compare_full(inputs, backend="tcgen05"):
+    """Element-wise errors of the library against the full oracle."""
+    o, lse = run_lib(inputs, backend)
+    o_ref, lse_ref = run_oracle(inputs)
+    return errors(f64(o), o_ref, lse.double().numpy(), lse_ref)
+
+
+def gather_rows(spec, o, lse, rows, cu_q=None):
+    """O rows [n, Dv] and LSE [n] of the library output at (b, h, i) triples."""
+    out_o, out_l = [], []
+    for b, h, i in rows:
+        if spec.varlen:
+            t = int(cu_q[b]) + i
+            out_o.append(o[t, h])
+            out_l.append(lse[h, t])
+        else:
+            out_o.append(o[b, i, h])
+            out_l.append(lse[b, h, i])
+    return f64(torch.stack(out_o)), torch.stack(out_l).double().numpy()

@@ -1,0 +1,148 @@
+"""The C-ABI library on the CPU: it loads, exports every function the header
+declares, validates arguments before touching a GPU, and its host copy of the
+persistent schedule visits every work tile exactly once, heaviest first."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import __graft_entry__
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    __graft_entry__.build()
+    import attention_forward_sm100_gb300 as m
+    return m
+
+
+def _header_functions():
+    text = open(os.path.join(ROOT, "include", "attn_fwd.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*[A-Za-z_][\w \*]*?\b(attn_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_function(pkg):
+    names = _header_functions()
+    assert {"attn_fwd", "attn_fwd_check", "attn_fwd_plan", "attn_fwd_schedule"} <= set(names)
+    lib = ctypes.CDLL(pkg._binding.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in attn_fwd.h but not exported"
+
+
+def test_params_layout(pkg):
+    assert pkg.lib().attn_fwd_params_size() == ctypes.sizeof(pkg.Params)
+
+
+def _meta(shape, dtype=torch.bfloat16):
+    # Shapes and strides only; plan() never dereferences pointers.
+    return torch.empty(shape, dtype=dtype, device="meta")
+
+
+class _Fake:
+    """Tensor stand-in with a chosen data_ptr, for host-side validation."""
+
+    def __init__(self, shape, dtype=torch.bfloat16, ptr=1 << 20, strides=None):
+        self.shape = torch.Size(shape)
+        self.dtype = dtype
+        self._ptr = ptr
+        t = torch.empty(shape, device="meta")
+        self._strides = strides or t.stride()
+
+    def data_ptr(self):
+        return self._ptr
+
+    def stride(self):
+        return self._strides
+
+    def numel(self):
+        n = 1
+        for s in self.shape:
+            n *= s
+        return n
+
+    def element_size(self):
+        return 1
+
+
+def _params(pkg, B=2, S=512, Hq=8, Hkv=2, D=128, Dv=128, causal=True, **kw):
+    q = _Fake((B, S, Hq, D), ptr=kw.pop("qptr", 1 << 20))
+    k = _Fake((B, S, Hkv, D), ptr=2 << 20)
+    v = _Fake((B, S, Hkv, Dv), ptr=3 << 20)
+    o = _Fake((B, S, Hq, Dv), ptr=4 << 20)
+    ws = _Fake((256,), dtype=torch.uint8, ptr=5 << 20)
+    return pkg.make_params(q, k, v, causal=causal, out=o, lse=None, workspace=ws, **kw)
+
+
+def test_plan_persistent(pkg):
+    info = pkg.plan(_params(pkg))
+    assert info.rows_per_tile == 256
+    assert info.work_tiles == 2 * 8 * 2
+    assert info.block == 512 and info.tmem_columns == 512
+    assert 0 < info.smem_bytes <= 232448
+    assert info.grid == min(info.work_tiles, 148) or info.grid <= info.work_tiles
+
+
+@pytest.mark.parametrize("bad", ["heads", "dims", "misaligned", "scale", "noworkspace"])
+def test_validation_rejects(pkg, bad):
+    if bad == "heads":
+        p = _params(pkg, Hq=6, Hkv=4)
+        want = 1
+    elif bad == "dims":
+        p = _params(pkg, D=96, Dv=96)
+        want = 2
+    elif bad == "misaligned":
+        p = _params(pkg, qptr=(1 << 20) + 2)
+        want = 1
+    elif bad == "scale":
+        p = _params(pkg)
+        p.softmax_scale = -1.0
+        want = 1
+    else:
+        p = _params(pkg)
+        p.workspace = None
+        want = 1
+    with pytest.raises(pkg.AttnError) as e:
+        pkg.plan(p)
+    assert e.value.status == want
+    assert pkg.last_error()
+
+
+def test_simple_backend_plan_accepts_odd_dims(pkg):
+    p = _params(pkg, D=96, Dv=80, backend="simple")
+    info = pkg.plan(p)
+    assert info.backend == 1
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv", [(1, 1, 1, 1), (2, 700, 8, 2), (3, 256, 4, 4), (1, 4096, 16, 16)])
+def test_schedule_fixed_covers_each_tile_once(pkg, B, S, Hq, Hkv):
+    p = _params(pkg, B=B, S=S, Hq=Hq, Hkv=Hkv)
+    order = pkg.schedule(p)
+    T = (S + 255) // 256
+    assert len(order) == B * Hq * T
+    assert set(order) == {(b, h, t) for b in range(B) for h in range(Hq) for t in range(T)}
+    g = Hq // Hkv
+    # heaviest first inside each (sequence, KV-head group), heads of a group interleaved
+    for b in range(B):
+        for hk in range(Hkv):
+            seq = [t for (bb, h, t) in order if bb == b and h // g == hk]
+            assert seq == sorted(seq, reverse=True)
+
+
+def test_schedule_packed(pkg):
+    lens = [2646, 7628, 1356, 5009, 4477, 3351, 2296, 891]
+    cu = [0]
+    for n in lens:
+        cu.append(cu[-1] + n)
+    p = _params(pkg, B=8, S=8192, Hq=32, Hkv=8)
+    order = pkg.schedule(p, host_cu_seqlens_q=cu)
+    expect = {(b, h, t) for b, n in enumerate(lens) for h in range(32) for t in range((n + 255) // 256)}
+    assert len(order) == len(expect) and set(order) == expect
+    # sequences in order
+    bs = [b for b, _, _ in order]
+    assert bs == sorted(bs)

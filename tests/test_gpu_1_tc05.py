@@ -1,0 +1,80 @@
+"""The tcgen05 kernel against the oracle on small shapes that span several
+tiles, ragged tails and the degenerate cases (single row, single key, empty
+key sequence, Sq != Sk)."""
+import numpy as np
+import pytest
+import torch
+
+from attention_forward_sm100_gb300 import workloads as W
+from helpers import assert_within, compare_full, f64, run_lib
+
+S = W.AttnSpec
+CASES = {
+    # name: spec
+    "d64_noncausal_s128": S(1, 2, 2, 128, 128, 64, 64, False, seed=0),
+    "d128_causal_s256": S(1, 2, 2, 256, 256, 128, 128, True, seed=31),
+    "d128_causal_s1": S(2, 2, 2, 1, 1, 128, 128, True, seed=32),
+    "d128_causal_s127": S(2, 2, 1, 127, 127, 128, 128, True, seed=33),
+    "d128_causal_s129": S(1, 4, 2, 129, 129, 128, 128, True, seed=34),
+    "d128_causal_s700": S(2, 2, 2, 700, 700, 128, 128, True, seed=35),
+    "d128_noncausal_s513": S(1, 3, 3, 513, 513, 128, 128, False, seed=36),
+    "d128_noncausal_sq200_sk333": S(2, 2, 1, 200, 333, 128, 128, False, seed=37),
+    "d128_noncausal_sk1": S(1, 2, 2, 300, 1, 128, 128, False, seed=38),
+    "d128_causal_sq300_sk170": S(1, 2, 2, 300, 170, 128, 128, True, seed=39),
+    "d64_causal_s1000": S(1, 2, 2, 1000, 1000, 64, 64, True, seed=40),
+    "d64_gqa_noncausal_s390": S(2, 8, 2, 390, 390, 64, 64, False, seed=41),
+    "packed_gqa_causal": S(4, 8, 2, 640, 640, 128, 128, True, seed=42, lengths_q=(1, 300, 129, 640)),
+    "packed_noncausal_qk_differ": S(3, 4, 4, 400, 400, 128, 128, False, seed=43, lengths_q=(257, 3, 130),
+                                    lengths_k=(5, 400, 128)),
+    "packed_noncausal_empty_k": S(2, 2, 2, 200, 200, 64, 64, False, seed=44, lengths_q=(200, 50),
+                                  lengths_k=(0, 70)),
+    "rope_causal_s300": S(1, 2, 2, 300, 300, 128, 128, True, seed=45, rope=64),
+    "rope_packed_causal": S(2, 4, 4, 260, 260, 128, 128, True, seed=46, rope=64, lengths_q=(260, 17)),
+    "fp8_causal_s300": S(1, 2, 2, 300, 300, 128, 128, True, seed=47, qk_dtype="fp8"),
+    "fp8_packed_noncausal": S(2, 4, 2, 400, 400, 128, 128, False, seed=48, qk_dtype="fp8", lengths_q=(400, 131)),
+}
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_tc05_matches_oracle(name):
+    spec = CASES[name]
+    err = compare_full(W.make_inputs(spec))
+    assert_within(err, spec.qk_dtype)
+
+
+@pytest.mark.gpu
+def test_causal_row0_is_exact():
+    """Row 0 of a causal sequence sees one key: O = V[0] bit for bit and
+    LSE = s_00 (the weight is exactly 1)."""
+    spec = S(2, 4, 2, 384, 384, 128, 128, True, seed=50)
+    inp = W.make_inputs(spec)
+    o, lse = run_lib(inp)
+    v0 = inp["v"][:, 0]                       # [B, Hkv, Dv]
+    exp = v0.repeat_interleave(2, dim=1)      # query heads 2g, 2g+1 -> kv head g
+    assert torch.equal(o[:, 0].view(torch.int16), exp.view(torch.int16))
+    q0 = f64(inp["q"][:, 0])
+    k0 = np.repeat(f64(inp["k"][:, 0]), 2, axis=1)
+    s00 = spec.softmax_scale * np.einsum("bhd,bhd->bh", q0, k0)
+    assert np.abs(lse[:, :, 0].double().numpy() - s00).max() < 1e-4
+
+
+@pytest.mark.gpu
+def test_repeated_calls_reuse_workspace():
+    """The persistent scheduler's counters reset after every call."""
+    spec = S(2, 4, 4, 1000, 1000, 128, 128, True, seed=51)
+    inp = W.make_inputs(spec)
+    o1, l1 = run_lib(inp)
+    o2, l2 = run_lib(inp)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1, l2)
+
+
+@pytest.mark.gpu
+def test_tc05_agrees_with_simple_kernel():
+    spec = S(2, 4, 2, 600, 600, 128, 128, True, seed=52)
+    inp = W.make_inputs(spec)
+    o1, l1 = run_lib(inp)
+    o2, l2 = run_lib(inp, backend="simple")
+    assert (o1.double() - o2.double()).abs().max().item() < 2e-2
+    assert (l1.double() - l2.double()).abs().max().item() < 1e-3
