@@ -132,6 +132,11 @@ int sm_count_cached() {
   return v;
 }
 
+int32_t kv_chunk_for(const attn_fwd_params* p) {
+  const int64_t row = (int64_t)(p->head_dim_qk * qk_elem_bytes(p)) + 2ll * p->rope_depth + 2ll * p->head_dim_v;
+  return af::choose_kv_chunk(p->seqlen_k, row, p->num_heads_kv, af::kL2ChunkBudget);
+}
+
 int64_t work_tiles_bound(const attn_fwd_params* p) {
   const int64_t T = af::tiles_for(p->seqlen_q, af::kRowsPerTile);
   return (int64_t)p->batch * p->num_heads_q * T;
@@ -225,6 +230,7 @@ attn_status launch_tc05(const attn_fwd_params* p, cudaStream_t stream) {
   prm.heads_kv = p->num_heads_kv;
   prm.group = p->num_heads_q / p->num_heads_kv;
   prm.tiles_per_seq = af::tiles_for(p->seqlen_q, af::kRowsPerTile);
+  prm.kv_chunk = kv_chunk_for(p);
   prm.total_work = packed ? 0 : work_tiles_bound(p);
   prm.packed = packed ? 1 : 0;
   prm.total_q = packed ? p->total_q : 0;
@@ -239,6 +245,14 @@ attn_status launch_tc05(const attn_fwd_params* p, cudaStream_t stream) {
 }
 
 }  // namespace
+
+attn_status af::report_error(attn_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
 
 extern "C" {
 
@@ -323,6 +337,7 @@ int64_t attn_fwd_schedule(const attn_fwd_params* p, const int32_t* host_cu_seqle
   clear_error();
   if (p == nullptr || p->num_heads_kv <= 0 || p->num_heads_q % p->num_heads_kv) return -1;
   const int group = p->num_heads_q / p->num_heads_kv;
+  const int32_t chunk = kv_chunk_for(p);
   int64_t n = 0;
   auto emit = [&](const af::WorkTile& w) {
     if (n < cap && out != nullptr) {
@@ -335,13 +350,14 @@ int64_t attn_fwd_schedule(const attn_fwd_params* p, const int32_t* host_cu_seqle
   if (host_cu_seqlens_q == nullptr) {
     const int32_t T = af::tiles_for(p->seqlen_q, af::kRowsPerTile);
     const int64_t total = (int64_t)p->batch * p->num_heads_q * T;
-    for (int64_t w = 0; w < total; ++w) emit(af::decode_fixed(w, T, p->num_heads_q, group));
+    for (int64_t w = 0; w < total; ++w) emit(af::decode_fixed(w, T, p->num_heads_q, group, chunk));
     return n;
   }
   for (int b = 0; b < p->batch; ++b) {
     const int32_t len = host_cu_seqlens_q[b + 1] - host_cu_seqlens_q[b];
     const int32_t T = af::tiles_for(len, af::kRowsPerTile);
-    for (int64_t wl = 0; wl < (int64_t)T * p->num_heads_q; ++wl) emit(af::decode_in_sequence(wl, b, T, group));
+    for (int64_t wl = 0; wl < (int64_t)T * p->num_heads_q; ++wl)
+      emit(af::decode_in_sequence(wl, b, T, group, p->num_heads_kv, chunk));
   }
   return n;
 }

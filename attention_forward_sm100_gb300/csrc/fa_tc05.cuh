@@ -7,17 +7,19 @@
 //     128-row Q tiles that ping-pong between two softmax warpgroups so the
 //     tensor core always has one Q tile's MMAs to run while the other tile's
 //     softmax runs;
-//   * warp 13 is the scheduler and the Q/K producer: it takes work indices
+//   * warp 14 is the scheduler and the Q/K producer: it takes work indices
 //     from an atomic counter, publishes each decoded work tile through a
 //     two-slot shared-memory ring (the shared work index of the scheduler
 //     page, initial_state / advance) and streams K tiles into a staged ring
 //     with TMA and transaction-count mbarriers (acquire / expect-bytes /
-//     commit of the producer-pipeline page); warp 14 streams V tiles into
+//     commit of the producer-pipeline page); warp 15 streams V tiles into
 //     their own ring. K is stored k-major and V mn-major, both with the
 //     128-byte swizzle, exactly as the MMAs read them;
-//   * warp 12 issues every tcgen05.mma from one thread: S_i = Q_i K^T into
-//     tensor memory (fp32), then O_i += P_i V with P_i (bf16) read from tensor
-//     memory where the softmax left it, over the S_i columns;
+//   * warps 12 and 13 each issue the tcgen05.mma of one Q tile from one
+//     thread: S_i = Q_i K^T into tensor memory (fp32), then O_i += P_i V with
+//     P_i (bf16) read from tensor memory where the softmax left it, over the
+//     S_i columns; one issuer per tile lets one tile's barrier waits overlap
+//     the other tile's MMAs;
 //   * warpgroups 0 and 1 own Q tiles 0 and 1: thread r owns row r (TMEM lane
 //     r), loads S, applies the causal / sequence-end mask, keeps the running
 //     max m and sum l in log2 units, writes P = 2^(s*c - m) as bf16 back to
@@ -52,8 +54,8 @@ enum BarId : int {
   BAR_Q_EMPTY = 2,       // last S MMA of a work tile done: Q region free
   BAR_S_FULL = 3,        // +i, S_i = Q_i K^T complete
   BAR_P_FULL = 5,        // +i, P_i written to tensor memory (128 arrivals)
-  BAR_ALPHA = 7,         // +i, alpha (or the final 1/l) of Q tile i in shared memory (128)
-  BAR_O_CORR = 9,        // +i, O_i rescaled for the next P V (128)
+  BAR_STATS = 7,         // +i, final 1/l of Q tile i in shared memory (128 arrivals)
+  BAR_UNUSED = 9,        // +i, spare
   BAR_O_FINAL = 11,      // +i, last P_i V of a work tile complete
   BAR_O_FREE = 13,       // +i, epilogue finished reading O_i (128)
   BAR_STATS_FREE = 15,   // +i, correction read the 1/l of Q tile i (128)
@@ -64,9 +66,9 @@ enum BarId : int {
   BAR_FIXED = 24         // then K_FULL[NK], K_EMPTY[NK], V_FULL[NV], V_EMPTY[NV]
 };
 
-// Consumers of a scheduler slot: MMA lane, 2 softmax warpgroups, the
+// Consumers of a scheduler slot: the two MMA lanes, 2 softmax warpgroups, the
 // correction warpgroup and the V producer lane.
-constexpr uint32_t kSchedConsumers = 1 + 128 + 128 + 128 + 1;
+constexpr uint32_t kSchedConsumers = 2 + 128 + 128 + 128 + 1;
 
 template <int DQK_, int DR_, int DV_, bool FP8_>
 struct Tc05Traits {
@@ -87,8 +89,7 @@ struct Tc05Traits {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = NQ * Q_TILE_BYTES;
   static constexpr int OFF_V = OFF_K + NK * K_STAGE_BYTES;
-  static constexpr int OFF_ALPHA = OFF_V + NV * V_STAGE_BYTES;      // float [NQ][BM]
-  static constexpr int OFF_RCPL = OFF_ALPHA + NQ * BM * 4;          // float [NQ][BM]
+  static constexpr int OFF_RCPL = OFF_V + NV * V_STAGE_BYTES;       // float [NQ][BM]
   static constexpr int OFF_KS = OFF_RCPL + NQ * BM * 4;             // float [NQ][2][BN] (fp8)
   static constexpr int KS_BYTES = FP8 ? NQ * 2 * BN * 4 : 0;
   static constexpr int OFF_SCHED = OFF_KS + KS_BYTES;               // 2 slots x 32 bytes
@@ -116,7 +117,7 @@ struct Tc05Traits {
   static constexpr uint32_t IDESC_PV = ptx::idesc_f32acc(1, 1, false, true, 128, DV);
 
   // Register split (setmaxnreg) of a 512-thread CTA launched with 128 registers per thread.
-  static constexpr int REG_SOFTMAX = 176, REG_CORR = 96, REG_MISC = 64;
+  static constexpr int REG_SOFTMAX = 184, REG_CORR = 80, REG_MISC = 64;
   static_assert(2 * 128 * REG_SOFTMAX + 128 * REG_CORR + 128 * REG_MISC <= 512 * 128,
                 "register split exceeds the launch allocation");
 };
@@ -144,7 +145,7 @@ __device__ __forceinline__ void raise_error(const Ctx& c, int role, int id) {
 // Warp-uniform bounded wait: every lane polls, the result is the same in all lanes.
 __device__ __forceinline__ bool wait_warp(const Ctx& c, int id, uint32_t parity, int role) {
   const uint32_t bar = c.bar(id);
-  if (__all_sync(kFull, ptx::mbar_try_wait(bar, parity))) return true;
+  if (__all_sync(kFull, ptx::mbar_test_wait(bar, parity))) return true;
   const uint64_t t0 = __shfl_sync(kFull, ptx::globaltimer(), 0);
   for (uint32_t it = 1;; ++it) {
     if (__all_sync(kFull, ptx::mbar_try_wait(bar, parity))) return true;
@@ -222,7 +223,7 @@ __device__ __forceinline__ SchedSlot decode_work(const Tc05Params& P, int64_t w,
   s.lk = P.seqlen_k;
   if (!P.packed) {
     if (w < P.total_work) {
-      const WorkTile wt = decode_fixed(w, P.tiles_per_seq, P.heads_q, P.group);
+      const WorkTile wt = decode_fixed(w, P.tiles_per_seq, P.heads_q, P.group, P.kv_chunk);
       s.valid = 1; s.b = wt.b; s.h = wt.h; s.t = wt.t;
     }
     return s;
@@ -245,7 +246,8 @@ __device__ __forceinline__ SchedSlot decode_work(const Tc05Params& P, int64_t w,
       cur.b += L;
       const int b = cur.b;
       const int qs = P.cu_q[b], qe = P.cu_q[b + 1], ks = P.cu_k[b], ke = P.cu_k[b + 1];
-      const WorkTile wt = decode_in_sequence(w - cur.base, b, tiles_for(qe - qs, kRowsPerTile), P.group);
+      const WorkTile wt =
+          decode_in_sequence(w - cur.base, b, tiles_for(qe - qs, kRowsPerTile), P.group, P.heads_kv, P.kv_chunk);
       s.valid = 1; s.b = b; s.h = wt.h; s.t = wt.t;
       s.q_start = qs; s.lq = qe - qs; s.k_start = ks; s.lk = ke - ks;
       return s;
@@ -388,159 +390,131 @@ __device__ void role_load_v(const Tc05Params& P, const Ctx& c) {
 // ---------------------------------------------------------------------------------------------
 template <class T>
 __device__ __forceinline__ void issue_s(const Ctx& c, int i, uint32_t kstage) {
+  constexpr uint32_t HI = ptx::sdesc_hi_sw128(1024);
   const uint32_t d = c.tmem + T::tm_s(i);
-  const uint32_t qa = ptx::opaque(c.sbase + T::OFF_Q + i * T::Q_TILE_BYTES);
-  const uint32_t ka = ptx::opaque(c.sbase + T::OFF_K + kstage * T::K_STAGE_BYTES);
+  const uint32_t qa = ptx::sdesc_lo(ptx::opaque(c.sbase + T::OFF_Q + i * T::Q_TILE_BYTES), 16);
+  const uint32_t ka = ptx::sdesc_lo(ptx::opaque(c.sbase + T::OFF_K + kstage * T::K_STAGE_BYTES), 16);
   if (T::FP8) {
 #pragma unroll
     for (int kk = 0; kk < T::DQK / 32; ++kk)
-      ptx::mma_fp8_ss(d, ptx::sdesc_sw128(qa + kk * 32, 16, 1024), ptx::sdesc_sw128(ka + kk * 32, 16, 1024),
-                      T::IDESC_S, kk > 0);
+      ptx::mma_fp8_ss_lo<HI, HI, T::IDESC_S>(d, qa + kk * 2, ka + kk * 2, kk > 0);
   } else {
 #pragma unroll
     for (int kk = 0; kk < T::DQK / 16; ++kk) {
-      const uint32_t off = (kk >> 2) * T::CHUNK_BYTES + (kk & 3) * 32;
-      ptx::mma_bf16_ss(d, ptx::sdesc_sw128(qa + off, 16, 1024), ptx::sdesc_sw128(ka + off, 16, 1024), T::IDESC_S,
-                       kk > 0);
+      const uint32_t off = ((kk >> 2) * T::CHUNK_BYTES + (kk & 3) * 32) >> 4;
+      ptx::mma_bf16_ss_lo<HI, HI, T::IDESC_S>(d, qa + off, ka + off, kk > 0);
     }
 #pragma unroll
     for (int kk = 0; kk < T::DR / 16; ++kk) {
-      const uint32_t off = T::QK_CHUNKS * T::CHUNK_BYTES + kk * 32;
-      ptx::mma_bf16_ss(d, ptx::sdesc_sw128(qa + off, 16, 1024), ptx::sdesc_sw128(ka + off, 16, 1024), T::IDESC_S,
-                       1u);
+      const uint32_t off = (T::QK_CHUNKS * T::CHUNK_BYTES + kk * 32) >> 4;
+      ptx::mma_bf16_ss_lo<HI, HI, T::IDESC_S>(d, qa + off, ka + off, 1u);
     }
   }
 }
 
 template <class T>
 __device__ __forceinline__ void issue_pv(const Ctx& c, int i, uint32_t vstage, bool accumulate) {
+  constexpr uint32_t HI = ptx::sdesc_hi_sw128(1024);
   const uint32_t d = c.tmem + T::tm_o(i);
   const uint32_t a = c.tmem + T::tm_s(i);
-  const uint32_t va = ptx::opaque(c.sbase + T::OFF_V + vstage * T::V_STAGE_BYTES);
+  const uint32_t va = ptx::sdesc_lo(ptx::opaque(c.sbase + T::OFF_V + vstage * T::V_STAGE_BYTES), T::CHUNK_BYTES);
 #pragma unroll
   for (int kk = 0; kk < kBlockN / 16; ++kk)
-    ptx::mma_bf16_ts(d, a + kk * 8, ptx::sdesc_sw128(va + kk * 2048, T::CHUNK_BYTES, 1024), T::IDESC_PV,
-                     (accumulate || kk > 0) ? 1u : 0u);
+    ptx::mma_bf16_ts_lo<HI, T::IDESC_PV>(d, a + kk * 8, va + kk * (2048 >> 4), (accumulate || kk > 0) ? 1u : 0u);
 }
 
+// One MMA-issuing warp per Q tile (warp 12 for tile 0, warp 13 for tile 1):
+// each issues S_i = Q_i K_j^T and O_i += P_i V_j for its own tile, so the
+// waits of one tile overlap the other tile's MMAs on the tensor core. K, V and
+// Q stages are released by one commit from each issuer.
 template <class T, bool CAUSAL>
-__device__ void role_mma(const Tc05Params& P, const Ctx& c) {
+__device__ void role_mma(const Tc05Params& P, const Ctx& c, const int i) {
   const bool leader = (threadIdx.x & 31) == 0;
+  const int role = kRoleMma;
   Ring<2> sched;
-  Ring<T::NK> kr;   // stage of the next K tile to consume
-  Ring<T::NV> vr;   // stage of the next V tile to consume
-  uint32_t q_full_phase = 0;
-  uint32_t p_phase = 0, ocorr_phase = 0, ofree_phase = 0;   // bit i: Q tile i
+  Ring<T::NK> kr;   // stage of the next K tile
+  Ring<T::NV> vr;   // stage of the next V tile
+  uint32_t q_full_phase = 0, p_phase = 0, ofree_phase = 0;
   bool aborted = false;
-#define AF_WAIT(id, par)                      \
-  if (!wait_warp(c, (id), (par), kRoleMma)) { \
-    aborted = true;                           \
-    break;                                    \
+#define AF_WAIT(id, par)                    \
+  if (!wait_warp(c, (id), (par), role)) {   \
+    aborted = true;                         \
+    break;                                  \
   }
   while (true) {
-    if (!wait_warp(c, BAR_SCHED_FULL + sched.idx, sched.phase, kRoleMma)) { aborted = true; break; }
+    if (!wait_warp(c, BAR_SCHED_FULL + sched.idx, sched.phase, role)) { aborted = true; break; }
     const SchedSlot s = read_slot(c, sched.idx, T::OFF_SCHED);
     if (leader) ptx::mbar_arrive(c.bar(BAR_SCHED_EMPTY + sched.idx));
     sched.next();
     if (!s.valid) break;
     const Geo g = tile_geo<CAUSAL>(s);
-    const int n0 = g.n[0], n1 = g.n[1];
+    const int n = g.n[i], n1 = g.n[1];
     if (n1 == 0) {
       // No keys: keep the per-tile O-free handshake in step with the epilogue.
-      AF_WAIT(BAR_O_FREE + 0, (ofree_phase & 1u) ^ 1u);
-      AF_WAIT(BAR_O_FREE + 1, ((ofree_phase >> 1) & 1u) ^ 1u);
-      ofree_phase ^= 3u;
+      AF_WAIT(BAR_O_FREE + i, ofree_phase ^ 1u);
+      ofree_phase ^= 1u;
       continue;
     }
-    // j = 0: S_0 of both Q tiles.
-    AF_WAIT(BAR_Q_FULL + 0, q_full_phase);
+    AF_WAIT(BAR_Q_FULL + i, q_full_phase);
+    q_full_phase ^= 1u;
+    // S_i(0)
     AF_WAIT(T::BAR_K_FULL + kr.idx, kr.phase);
     ptx::tc_fence_after();
     if (leader) {
-      issue_s<T>(c, 0, kr.idx);
-      ptx::mma_commit(c.bar(BAR_S_FULL + 0));
-    }
-    __syncwarp();
-    AF_WAIT(BAR_Q_FULL + 1, q_full_phase);
-    q_full_phase ^= 1u;
-    ptx::tc_fence_after();
-    if (leader) {
-      issue_s<T>(c, 1, kr.idx);
-      ptx::mma_commit(c.bar(BAR_S_FULL + 1));
+      issue_s<T>(c, i, kr.idx);
+      ptx::mma_commit(c.bar(BAR_S_FULL + i));
       ptx::mma_commit(c.bar(T::BAR_K_EMPTY + kr.idx));
-      if (n1 == 1) ptx::mma_commit(c.bar(BAR_Q_EMPTY));
+      if (n == 1) ptx::mma_commit(c.bar(BAR_Q_EMPTY));
     }
     __syncwarp();
     kr.next();
-    for (int j = 1; j <= n1; ++j) {
-      const int jp = j - 1;
-      bool v_ready = false, k_ready = false;
-      if (jp < n0) {  // O_0 += P_0 V_{j-1}
-        AF_WAIT(BAR_P_FULL + 0, p_phase & 1u);
-        p_phase ^= 1u;
-        if (jp == 0) {
-          AF_WAIT(BAR_O_FREE + 0, (ofree_phase & 1u) ^ 1u);
-          ofree_phase ^= 1u;
-        } else {
-          AF_WAIT(BAR_O_CORR + 0, ocorr_phase & 1u);
-          ocorr_phase ^= 1u;
-        }
-        AF_WAIT(T::BAR_V_FULL + vr.idx, vr.phase);
-        v_ready = true;
-        ptx::tc_fence_after();
-        if (leader) {
-          issue_pv<T>(c, 0, vr.idx, jp > 0);
-          if (jp == n0 - 1) ptx::mma_commit(c.bar(BAR_O_FINAL + 0));
-        }
-        __syncwarp();
+    for (int j = 1; j <= n; ++j) {
+      // O_i += P_i V_{j-1}
+      AF_WAIT(BAR_P_FULL + i, p_phase);
+      p_phase ^= 1u;
+      if (j == 1) {
+        AF_WAIT(BAR_O_FREE + i, ofree_phase ^ 1u);
+        ofree_phase ^= 1u;
       }
-      if (j < n0) {  // S_0 = Q_0 K_j^T
+      AF_WAIT(T::BAR_V_FULL + vr.idx, vr.phase);
+      ptx::tc_fence_after();
+      if (leader) {
+        issue_pv<T>(c, i, vr.idx, j > 1);
+        ptx::mma_commit(c.bar(T::BAR_V_EMPTY + vr.idx));
+        if (j == n) ptx::mma_commit(c.bar(BAR_O_FINAL + i));
+      }
+      __syncwarp();
+      vr.next();
+      if (j < n) {  // S_i = Q_i K_j^T
         AF_WAIT(T::BAR_K_FULL + kr.idx, kr.phase);
-        k_ready = true;
         ptx::tc_fence_after();
         if (leader) {
-          issue_s<T>(c, 0, kr.idx);
-          ptx::mma_commit(c.bar(BAR_S_FULL + 0));
-        }
-        __syncwarp();
-      }
-      {  // O_1 += P_1 V_{j-1}
-        AF_WAIT(BAR_P_FULL + 1, (p_phase >> 1) & 1u);
-        p_phase ^= 2u;
-        if (jp == 0) {
-          AF_WAIT(BAR_O_FREE + 1, ((ofree_phase >> 1) & 1u) ^ 1u);
-          ofree_phase ^= 2u;
-        } else {
-          AF_WAIT(BAR_O_CORR + 1, (ocorr_phase >> 1) & 1u);
-          ocorr_phase ^= 2u;
-        }
-        if (!v_ready) AF_WAIT(T::BAR_V_FULL + vr.idx, vr.phase);
-        ptx::tc_fence_after();
-        if (leader) {
-          issue_pv<T>(c, 1, vr.idx, jp > 0);
-          ptx::mma_commit(c.bar(T::BAR_V_EMPTY + vr.idx));
-          if (jp == n1 - 1) ptx::mma_commit(c.bar(BAR_O_FINAL + 1));
-        }
-        __syncwarp();
-        vr.next();
-      }
-      if (j < n1) {  // S_1 = Q_1 K_j^T
-        if (!k_ready) AF_WAIT(T::BAR_K_FULL + kr.idx, kr.phase);
-        ptx::tc_fence_after();
-        if (leader) {
-          issue_s<T>(c, 1, kr.idx);
-          ptx::mma_commit(c.bar(BAR_S_FULL + 1));
+          issue_s<T>(c, i, kr.idx);
+          ptx::mma_commit(c.bar(BAR_S_FULL + i));
           ptx::mma_commit(c.bar(T::BAR_K_EMPTY + kr.idx));
-          if (j == n1 - 1) ptx::mma_commit(c.bar(BAR_Q_EMPTY));
+          if (j == n - 1) ptx::mma_commit(c.bar(BAR_Q_EMPTY));
         }
         __syncwarp();
         kr.next();
       }
     }
     if (aborted) break;
+    // K/V tiles only the other Q tile visits: release this issuer's share.
+    for (int j = n; j < n1; ++j) {
+      AF_WAIT(T::BAR_K_FULL + kr.idx, kr.phase);
+      if (leader) ptx::mma_commit(c.bar(T::BAR_K_EMPTY + kr.idx));
+      __syncwarp();
+      kr.next();
+      AF_WAIT(T::BAR_V_FULL + vr.idx, vr.phase);
+      if (leader) ptx::mma_commit(c.bar(T::BAR_V_EMPTY + vr.idx));
+      __syncwarp();
+      vr.next();
+    }
+    if (aborted) break;
   }
 #undef AF_WAIT
-  // Drain: the arrive of this commit follows every MMA and commit issued before it.
+  // Drain: the arrive of this commit follows every MMA and commit this thread
+  // issued (both issuers commit; the phase completes after both).
   if (leader) {
     ptx::mma_commit(c.bar(BAR_DRAIN));
     wait_drain(c, BAR_DRAIN, 0);
@@ -555,7 +529,7 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
   const int tid = threadIdx.x - 128 * i;          // row of the Q tile == TMEM lane
   const uint32_t lane_base = (uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16;
   const uint32_t tS = c.tmem + lane_base + T::tm_s(i);
-  float* alpha_sm = reinterpret_cast<float*>(c.smem + T::OFF_ALPHA) + i * kBlockM;
+  const uint32_t tO = c.tmem + lane_base + T::tm_o(i);
   float* rcpl_sm = reinterpret_cast<float*>(c.smem + T::OFF_RCPL) + i * kBlockM;
   float* ks_sm = reinterpret_cast<float*>(c.smem + T::OFF_KS) + i * 2 * kBlockN;
   const int role = i == 0 ? kRoleSoftmax0 : kRoleSoftmax1;
@@ -601,24 +575,24 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
       ptx::tc_fence_after();
       float sv[128];
       {
-        uint32_t r[32];
+        uint32_t r[4][32];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          ptx::tmem_ld32(tS + 32 * q, r);
-          ptx::tmem_wait_ld();
+        for (int q = 0; q < 4; ++q) ptx::tmem_ld32(tS + 32 * q, r[q]);
+        ptx::tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) sv[32 * q + e] = __uint_as_float(r[e]);
-        }
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) sv[32 * q + e] = __uint_as_float(r[q][e]);
       }
       if (T::FP8) {
-        const float4* k4 = reinterpret_cast<const float4*>(ks_sm + (j & 1) * kBlockN);
+        const float2* k2 = reinterpret_cast<const float2*>(ks_sm + (j & 1) * kBlockN);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float4 kv = k4[e];
-          sv[4 * e + 0] *= kv.x;
-          sv[4 * e + 1] *= kv.y;
-          sv[4 * e + 2] *= kv.z;
-          sv[4 * e + 3] *= kv.w;
+        for (int e = 0; e < 64; ++e) {
+          const float2 kv = k2[e];
+          float a0, a1;
+          ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(sv[2 * e], sv[2 * e + 1]), ptx::f2_pack(kv.x, kv.y)), a0, a1);
+          sv[2 * e] = a0;
+          sv[2 * e + 1] = a1;
         }
       }
       const bool need_mask = (kb + kBlockN > s.lk) || (CAUSAL && kb + kBlockN - 1 > first_row);
@@ -628,15 +602,18 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
         for (int e = 0; e < 128; ++e)
           if (e >= vis) sv[e] = -INFINITY;
       }
-      float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
+      float mx0 = ptx::max3(sv[0], sv[1], sv[2]), mx1 = ptx::max3(sv[3], sv[4], sv[5]);
+      float mx2 = ptx::max3(sv[6], sv[7], sv[8]), mx3 = ptx::max3(sv[9], sv[10], sv[11]);
 #pragma unroll
-      for (int e = 4; e < 128; e += 4) {
-        mx0 = fmaxf(mx0, sv[e]);
-        mx1 = fmaxf(mx1, sv[e + 1]);
-        mx2 = fmaxf(mx2, sv[e + 2]);
-        mx3 = fmaxf(mx3, sv[e + 3]);
+      for (int e = 12; e < 124; e += 8) {
+        mx0 = ptx::max3(mx0, sv[e], sv[e + 1]);
+        mx1 = ptx::max3(mx1, sv[e + 2], sv[e + 3]);
+        mx2 = ptx::max3(mx2, sv[e + 4], sv[e + 5]);
+        mx3 = ptx::max3(mx3, sv[e + 6], sv[e + 7]);
       }
-      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c_row;
+      mx0 = ptx::max3(mx0, sv[124], sv[125]);
+      mx1 = ptx::max3(mx1, sv[126], sv[127]);
+      const float mx = ptx::max3(mx0, mx1, fmaxf(mx2, mx3)) * c_row;
       const float m_new = fmaxf(m, mx);
       float m_use = m, alpha = 1.f;
       if (j == 0) {
@@ -645,25 +622,41 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
         m_use = m_new;
         alpha = ptx::ex2(m - m_new);
       }
-      if (j > 0) {
-        alpha_sm[tid] = alpha;
-        ptx::mbar_arrive(c.bar(BAR_ALPHA + i));
-      }
-      const float neg = -m_use;
-      float s0 = 0.f, s1 = 0.f;
+      const uint64_t c2 = ptx::f2_pack(c_row, c_row);
+      const uint64_t n2 = ptx::f2_pack(-m_use, -m_use);
+      uint64_t acc0 = 0, acc1 = 0;   // (+0.0f, +0.0f) pairs
       uint32_t pk[64];
 #pragma unroll
       for (int e = 0; e < 64; ++e) {
-        const float p0 = ptx::ex2(fmaf(sv[2 * e], c_row, neg));
-        const float p1 = ptx::ex2(fmaf(sv[2 * e + 1], c_row, neg));
-        s0 += p0;
-        s1 += p1;
+        float x0, x1;
+        ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(sv[2 * e], sv[2 * e + 1]), c2, n2), x0, x1);
+        const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+        if (e & 1) acc1 = ptx::f2_add(acc1, ptx::f2_pack(p0, p1));
+        else acc0 = ptx::f2_add(acc0, ptx::f2_pack(p0, p1));
         pk[e] = ptx::pack_bf16(p0, p1);
       }
-      l = l * alpha + (s0 + s1);
+      float s0, s1, s2, s3;
+      ptx::f2_unpack(acc0, s0, s1);
+      ptx::f2_unpack(acc1, s2, s3);
+      l = l * alpha + ((s0 + s1) + (s2 + s3));
       ptx::tmem_st32(tS, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
       ptx::tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
       ptx::tmem_wait_st();
+      // Correction: the running max moved (rare with the 2^8 headroom), so
+      // rescale this warp's rows of O_i before the next P V accumulates into
+      // it. P_i(j-1) V was complete when S_i(j) arrived (same issuer, in order).
+      if (__any_sync(kFull, alpha != 1.f)) {
+#pragma unroll 1
+        for (int q = 0; q < T::DV / 32; ++q) {
+          uint32_t r[32];
+          ptx::tmem_ld32(tO + 32 * q, r);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+          ptx::tmem_st32(tO + 32 * q, r);
+        }
+        ptx::tmem_wait_st();
+      }
       ptx::tc_fence_before();
       ptx::mbar_arrive(c.bar(BAR_P_FULL + i));
       m = m_use;
@@ -677,7 +670,7 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
     if (!wait_warp(c, BAR_STATS_FREE + i, stats_phase ^ 1u, role)) return;
     stats_phase ^= 1u;
     rcpl_sm[tid] = l > 0.f ? 1.f / l : 0.f;
-    ptx::mbar_arrive(c.bar(BAR_ALPHA + i));
+    ptx::mbar_arrive(c.bar(BAR_STATS + i));
   }
 }
 
@@ -697,10 +690,9 @@ template <class T, bool CAUSAL>
 __device__ void role_correction(const Tc05Params& P, const Ctx& c) {
   const int tid = threadIdx.x - 256;
   const uint32_t lane_base = (uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16;
-  const float* alpha_sm = reinterpret_cast<const float*>(c.smem + T::OFF_ALPHA);
   const float* rcpl_sm = reinterpret_cast<const float*>(c.smem + T::OFF_RCPL);
   Ring<2> sched;
-  uint32_t alpha_phase[2] = {0, 0}, ofinal_phase[2] = {0, 0};
+  uint32_t stats_phase[2] = {0, 0}, ofinal_phase[2] = {0, 0};
   while (true) {
     if (!wait_warp(c, BAR_SCHED_FULL + sched.idx, sched.phase, kRoleCorrection)) return;
     const SchedSlot s = read_slot(c, sched.idx, T::OFF_SCHED);
@@ -708,33 +700,11 @@ __device__ void role_correction(const Tc05Params& P, const Ctx& c) {
     sched.next();
     if (!s.valid) return;
     const Geo g = tile_geo<CAUSAL>(s);
-
-    auto correct = [&](int i) -> bool {
-      if (!wait_warp(c, BAR_ALPHA + i, alpha_phase[i], kRoleCorrection)) return false;
-      alpha_phase[i] ^= 1u;
-      const float a = alpha_sm[i * kBlockM + tid];
-      if (__any_sync(kFull, a != 1.f)) {
-        ptx::tc_fence_after();
-        const uint32_t tO = c.tmem + lane_base + T::tm_o(i);
-#pragma unroll
-        for (int q = 0; q < T::DV / 32; ++q) {
-          uint32_t r[32];
-          ptx::tmem_ld32(tO + 32 * q, r);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * a);
-          ptx::tmem_st32(tO + 32 * q, r);
-        }
-        ptx::tmem_wait_st();
-      }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(c.bar(BAR_O_CORR + i));
-      return true;
-    };
-
-    auto epilogue = [&](int i) -> bool {
-      if (!wait_warp(c, BAR_ALPHA + i, alpha_phase[i], kRoleCorrection)) return false;
-      alpha_phase[i] ^= 1u;
+#pragma unroll 1
+    for (int i = 0; i < 2; ++i) {
+      // Epilogue of Q tile i: O = O / l, rounded once to bf16, stored row by row.
+      if (!wait_warp(c, BAR_STATS + i, stats_phase[i], kRoleCorrection)) return;
+      stats_phase[i] ^= 1u;
       const float rl = rcpl_sm[i * kBlockM + tid];
       ptx::mbar_arrive(c.bar(BAR_STATS_FREE + i));
       const int qi = g.q0 + kBlockM * i + tid;
@@ -742,7 +712,7 @@ __device__ void role_correction(const Tc05Params& P, const Ctx& c) {
       uint16_t* orow = P.o + (int64_t)s.b * P.o_stride_b + (int64_t)(s.q_start + qi) * P.o_stride_t +
                        (int64_t)s.h * P.o_stride_h;
       if (g.n[i] > 0) {
-        if (!wait_warp(c, BAR_O_FINAL + i, ofinal_phase[i], kRoleCorrection)) return false;
+        if (!wait_warp(c, BAR_O_FINAL + i, ofinal_phase[i], kRoleCorrection)) return;
         ofinal_phase[i] ^= 1u;
         ptx::tc_fence_after();
         const uint32_t tO = c.tmem + lane_base + T::tm_o(i);
@@ -760,23 +730,6 @@ __device__ void role_correction(const Tc05Params& P, const Ctx& c) {
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(c.bar(BAR_O_FREE + i));
-      return true;
-    };
-
-    const int n1 = g.n[1];
-    if (n1 == 0) {
-      if (!epilogue(0) || !epilogue(1)) return;
-      continue;
-    }
-    for (int jj = 1; jj <= n1; ++jj) {
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        if (jj < g.n[i]) {
-          if (!correct(i)) return;
-        } else if (jj == g.n[i]) {
-          if (!epilogue(i)) return;
-        }
-      }
     }
   }
 }
@@ -811,8 +764,8 @@ __global__ void __launch_bounds__(512, 1) fa_tc05_kernel(const __grid_constant__
       ptx::mbar_init(c.bar(BAR_Q_FULL + i), 1);
       ptx::mbar_init(c.bar(BAR_S_FULL + i), 1);
       ptx::mbar_init(c.bar(BAR_P_FULL + i), 128);
-      ptx::mbar_init(c.bar(BAR_ALPHA + i), 128);
-      ptx::mbar_init(c.bar(BAR_O_CORR + i), 128);
+      ptx::mbar_init(c.bar(BAR_STATS + i), 128);
+      ptx::mbar_init(c.bar(BAR_UNUSED + i), 1);
       ptx::mbar_init(c.bar(BAR_O_FINAL + i), 1);
       ptx::mbar_init(c.bar(BAR_O_FREE + i), 128);
       ptx::mbar_init(c.bar(BAR_STATS_FREE + i), 128);
@@ -820,17 +773,17 @@ __global__ void __launch_bounds__(512, 1) fa_tc05_kernel(const __grid_constant__
       ptx::mbar_init(c.bar(BAR_SCHED_FULL + i), 1);
       ptx::mbar_init(c.bar(BAR_SCHED_EMPTY + i), kSchedConsumers);
     }
-    ptx::mbar_init(c.bar(BAR_Q_EMPTY), 1);
-    ptx::mbar_init(c.bar(BAR_DRAIN), 1);
+    ptx::mbar_init(c.bar(BAR_Q_EMPTY), 2);
+    ptx::mbar_init(c.bar(BAR_DRAIN), 2);
 #pragma unroll
     for (int s = 0; s < T::NK; ++s) {
       ptx::mbar_init(c.bar(T::BAR_K_FULL + s), 1);
-      ptx::mbar_init(c.bar(T::BAR_K_EMPTY + s), 1);
+      ptx::mbar_init(c.bar(T::BAR_K_EMPTY + s), 2);
     }
 #pragma unroll
     for (int s = 0; s < T::NV; ++s) {
       ptx::mbar_init(c.bar(T::BAR_V_FULL + s), 1);
-      ptx::mbar_init(c.bar(T::BAR_V_EMPTY + s), 1);
+      ptx::mbar_init(c.bar(T::BAR_V_EMPTY + s), 2);
     }
     *c.abort_flag = 0;
     ptx::fence_mbar_init();
@@ -839,7 +792,7 @@ __global__ void __launch_bounds__(512, 1) fa_tc05_kernel(const __grid_constant__
     ptx::tmem_alloc(c.sbase + T::OFF_TMEM_SLOT, T::TMEM_COLS);
     ptx::tmem_relinquish();
   }
-  if (warp == 13 && lane == 0) {
+  if (warp == 14 && lane == 0) {
     ptx::prefetch_tmap(&P.tm_q);
     ptx::prefetch_tmap(&P.tm_k);
     ptx::prefetch_tmap(&P.tm_v);
@@ -862,9 +815,9 @@ __global__ void __launch_bounds__(512, 1) fa_tc05_kernel(const __grid_constant__
     role_correction<T, CAUSAL>(P, c);
   } else {
     setmaxnreg_dec<T::REG_MISC>();
-    if (warp == 12) role_mma<T, CAUSAL>(P, c);
-    else if (warp == 13) role_load_qk<T, CAUSAL>(P, c);
-    else if (warp == 14) role_load_v<T, CAUSAL>(P, c);
+    if (warp == 12 || warp == 13) role_mma<T, CAUSAL>(P, c, warp - 12);
+    else if (warp == 14) role_load_qk<T, CAUSAL>(P, c);
+    else role_load_v<T, CAUSAL>(P, c);
   }
 
   ptx::tc_fence_before();

@@ -11,6 +11,7 @@ namespace af {
 constexpr int kRowsPerTile = 256;   // query rows per work tile of the tcgen05 kernel
 constexpr int kBlockM = 128;        // query rows per MMA tile (one TMEM lane per row)
 constexpr int kBlockN = 128;        // keys per K/V tile
+constexpr int64_t kL2ChunkBudget = 48ll << 20;   // K/V bytes one scheduling chunk may keep in L2
 
 // Workspace words (uint32 each).
 enum WorkspaceWord : int {
@@ -44,6 +45,7 @@ struct Tc05Params {
   int64_t o_stride_b, o_stride_t, o_stride_h;  // elements
   int32_t batch, seqlen_q, seqlen_k, heads_q, heads_kv, group;
   int32_t tiles_per_seq;   // fixed length: ceil(Sq / kRowsPerTile)
+  int32_t kv_chunk;        // KV heads per scheduling chunk
   int64_t total_work;      // fixed length: exact number of work tiles
   int32_t packed;
   int32_t total_q;         // packed: rows of q (LSE and q_scale layout [Hq, Tq])
@@ -67,6 +69,10 @@ struct Tc05Config {
   int threads;
   int tmem_cols;
 };
+
+// Records the calling thread's last-error text (attn_fwd_last_error) and
+// returns `st`.
+attn_status report_error(attn_status st, const char* fmt, ...);
 
 // Static configuration of a variant (host).
 Tc05Config tc05_config(int variant);

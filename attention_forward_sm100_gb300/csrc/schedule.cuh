@@ -6,11 +6,12 @@
 // ROWS_PER_TILE query rows of one (sequence b, query head h). Work indices are
 // handed out by an atomic counter; index w decodes as follows:
 //   * sequences in order (packed inputs: b-major with a cursor over cu_seqlens);
-//   * inside a sequence, groups of query heads that share one KV head, so the
-//     heads reading the same K/V tiles run at the same time and share L2;
-//   * inside a group, query tiles from the last (most keys under a causal
-//     mask) to the first, heads of the group interleaved: the heaviest tiles
-//     are taken first and the light ones fill the tail.
+//   * inside a sequence, KV heads in chunks of kv_chunk heads, sized so the
+//     K/V of one chunk stays in L2 while its tiles are processed;
+//   * inside a chunk, query tiles from the last (most keys under a causal
+//     mask) to the first, and for each tile index every query head of the
+//     chunk, the heads that share one KV head next to each other: the
+//     heaviest tiles are taken first and the light ones fill the tail.
 #pragma once
 #include <stdint.h>
 
@@ -31,22 +32,36 @@ struct WorkTile {
 AF_HD inline int32_t tiles_for(int32_t len, int32_t rows) { return (len + rows - 1) / rows; }
 
 // Work index local to one sequence (0 <= wl < T * Hq) -> (h, t).
-AF_HD inline WorkTile decode_in_sequence(int64_t wl, int32_t b, int32_t T, int32_t group) {
-  const int64_t per_group = (int64_t)T * group;
-  const int32_t grp = (int32_t)(wl / per_group);
-  const int32_t rem = (int32_t)(wl - (int64_t)grp * per_group);
+AF_HD inline WorkTile decode_in_sequence(int64_t wl, int32_t b, int32_t T, int32_t group, int32_t heads_kv,
+                                         int32_t kv_chunk) {
+  const int64_t chunk_units = (int64_t)T * kv_chunk * group;
+  const int32_t c = (int32_t)(wl / chunk_units);
+  const int32_t r = (int32_t)(wl - (int64_t)c * chunk_units);
+  const int32_t kv_lo = c * kv_chunk;
+  const int32_t kv_n = heads_kv - kv_lo < kv_chunk ? heads_kv - kv_lo : kv_chunk;
+  const int32_t per_t = kv_n * group;
   WorkTile w;
   w.b = b;
-  w.h = grp * group + rem % group;
-  w.t = T - 1 - rem / group;
+  w.t = T - 1 - r / per_t;
+  w.h = kv_lo * group + r % per_t;
   return w;
 }
 
 // Fixed-length decode: every sequence has T tiles per head.
-AF_HD inline WorkTile decode_fixed(int64_t w, int32_t T, int32_t heads_q, int32_t group) {
+AF_HD inline WorkTile decode_fixed(int64_t w, int32_t T, int32_t heads_q, int32_t group, int32_t kv_chunk) {
   const int64_t per_seq = (int64_t)T * heads_q;
   const int32_t b = (int32_t)(w / per_seq);
-  return decode_in_sequence(w - (int64_t)b * per_seq, b, T, group);
+  return decode_in_sequence(w - (int64_t)b * per_seq, b, T, group, heads_q / group, kv_chunk);
+}
+
+// KV heads per chunk: as many as keep the chunk's K/V (seqlen_k rows of
+// k_row_bytes + v_row_bytes per head) within l2_budget bytes.
+AF_HD inline int32_t choose_kv_chunk(int64_t seqlen_k, int64_t kv_row_bytes, int32_t heads_kv, int64_t l2_budget) {
+  const int64_t per_head = seqlen_k * kv_row_bytes;
+  int64_t c = per_head > 0 ? l2_budget / per_head : heads_kv;
+  if (c < 1) c = 1;
+  if (c > heads_kv) c = heads_kv;
+  return (int32_t)c;
 }
 
 }  // namespace af

@@ -211,6 +211,11 @@ def max_over_ranks(x, world, device):
     return float(t.item())
 
 
+def whole_job_tflops(flops_per_rank, world, ms):
+    """Whole-job throughput: every rank ran flops_per_rank in at most ms."""
+    return flops_per_rank * world / (ms * 1e-3) / 1e12
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -219,7 +224,7 @@ def barrier(world):
 
 def run_reference(args, spec, world, rank):
     """Reference arm: the CPU oracle as it stands, one bounded sample of the
-    workload per step."""
+    workload per step. Under torchrun only rank 0 runs and prints."""
     if rank != 0:
         return
     from attention_forward_sm100_gb300 import workloads as W
@@ -250,10 +255,11 @@ def main():
     args = parse_args()
     from attention_forward_sm100_gb300 import workloads as W
     spec = W.WORKLOADS[args.workload]
-    world, rank, local = dist_setup(args)
     if args.impl == "reference":
-        run_reference(args, spec, world, rank)
+        # No process group: the reference arm never communicates.
+        run_reference(args, spec, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
         return
+    world, rank, local = dist_setup(args)
 
     import torch
 
@@ -304,7 +310,7 @@ def main():
     total_ms = max_over_ranks(total_ms, world, dev)
     ms = total_ms / args.steps
     flops = spec.flops()
-    value = flops * world / (ms * 1e-3) / 1e12
+    value = whole_job_tflops(flops, world, ms)
     kernel_ms = statistics.mean(per_launch)
     achieved = flops / (kernel_ms * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
@@ -344,7 +350,7 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world, dev)
-        e2e = {"value": flops * world / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+        e2e = {"value": whole_job_tflops(flops, world, e_ms), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
 
     cpu = None

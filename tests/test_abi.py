@@ -127,11 +127,31 @@ def test_schedule_fixed_covers_each_tile_once(pkg, B, S, Hq, Hkv):
     assert len(order) == B * Hq * T
     assert set(order) == {(b, h, t) for b in range(B) for h in range(Hq) for t in range(T)}
     g = Hq // Hkv
-    # heaviest first inside each (sequence, KV-head group), heads of a group interleaved
+    # heaviest first inside each (sequence, KV head)
     for b in range(B):
         for hk in range(Hkv):
             seq = [t for (bb, h, t) in order if bb == b and h // g == hk]
             assert seq == sorted(seq, reverse=True)
+    # the query heads of one KV head come back to back for each tile index
+    for n in range(0, len(order), g):
+        blk = order[n:n + g]
+        assert len({(b, h // g, t) for b, h, t in blk}) == 1
+
+
+def test_schedule_chunks_are_heaviest_first(pkg):
+    # 128 KV heads of 2 MB K/V each: several L2-sized chunks per sequence;
+    # inside a chunk the tile index never increases.
+    p = _params(pkg, B=1, S=4096, Hq=128, Hkv=128)
+    order = pkg.schedule(p)
+    heads_seen = []
+    ts = [t for _, _, t in order]
+    chunk_starts = [i for i in range(1, len(order)) if ts[i] > ts[i - 1]]
+    assert 1 <= len(chunk_starts) < 16
+    bounds = [0] + chunk_starts + [len(order)]
+    for a, e in zip(bounds[:-1], bounds[1:]):
+        assert ts[a:e] == sorted(ts[a:e], reverse=True)
+        heads_seen.append({h for _, h, _ in order[a:e]})
+    assert set().union(*heads_seen) == set(range(128))
 
 
 def test_schedule_packed(pkg):
