@@ -61,6 +61,10 @@ typedef enum attn_backend {
  * scheduler's work counter and the device error record. */
 #define ATTN_FWD_WORKSPACE_BYTES 256
 
+/* Size of the scratch array that attn_fwd_noalloc keeps inside the library
+ * (one copy per GPU that loads the library). */
+#define ATTN_FWD_STATIC_WORKSPACE_BYTES 256
+
 typedef struct attn_fwd_params {
   /* ---- tensors (device pointers, caller-owned) ------------------------- */
   const void *q;        /* fixed [B,Sq,Hq,Dqk] / packed [Tq,Hq,Dqk]; bf16 or fp8 (qk_dtype) */
@@ -137,6 +141,22 @@ size_t attn_fwd_workspace_bytes(const attn_fwd_params *p);
 /* Validates `p` and enqueues the forward on `stream`. Asynchronous. Errors:
  * INVALID_ARG / UNSUPPORTED before launch; CUDA if the launch failed. */
 attn_status attn_fwd(const attn_fwd_params *p, attn_stream_t stream);
+
+/* attn_fwd for callers that cannot allocate device memory: it takes no
+ * workspace (p->workspace is ignored) and uses a fixed scratch array of
+ * ATTN_FWD_STATIC_WORKSPACE_BYTES inside the library instead. The paper has
+ * no counterpart of this call; it exists for code that only receives tensors
+ * and a stream from a host framework that owns all device memory, or that
+ * must not allocate once it is running. It allocates nothing and calls no
+ * allocating routine. The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress, with that device current), so make it
+ * before any stream capture. Every call clears and reuses the same array:
+ * calls that overlap on the GPU (concurrent streams, or other threads) race
+ * on it and must be serialised by the caller. Device-side wait timeouts of
+ * this variant are not reported (there is no caller-visible error record).
+ * Returns UNSUPPORTED if a call would need more scratch than the array holds,
+ * otherwise as attn_fwd. */
+attn_status attn_fwd_noalloc(const attn_fwd_params *p, attn_stream_t stream);
 
 /* Synchronises `stream`, reads and clears the device error record of
  * `workspace`. Returns DEVICE_TIMEOUT if a kernel wait ran out, CUDA for a
