@@ -53,17 +53,18 @@ enum BarId : int {
   BAR_Q_FULL = 0,        // +i, TMA transaction barrier of Q tile i
   BAR_Q_EMPTY = 2,       // last S MMA of a work tile done: Q region free
   BAR_S_FULL = 3,        // +i, S_i = Q_i K^T complete
-  BAR_P_FULL = 5,        // +i, P_i written to tensor memory (128 arrivals)
+  BAR_P_LO = 5,          // +i, first half of P_i (keys 0..63) in tensor memory (128 arrivals)
   BAR_STATS = 7,         // +i, final 1/l of Q tile i in shared memory (128 arrivals)
-  BAR_UNUSED = 9,        // +i, spare
+  BAR_P_HI = 9,          // +i, second half of P_i (keys 64..127) in tensor memory (128)
   BAR_O_FINAL = 11,      // +i, last P_i V of a work tile complete
   BAR_O_FREE = 13,       // +i, epilogue finished reading O_i (128)
   BAR_STATS_FREE = 15,   // +i, correction read the 1/l of Q tile i (128)
   BAR_KS = 17,           // +i, fp8 k-scale tile written by the softmax warpgroup (128)
   BAR_SCHED_FULL = 19,   // +slot
   BAR_SCHED_EMPTY = 21,  // +slot
-  BAR_DRAIN = 23,        // final commit of the MMA thread
-  BAR_FIXED = 24         // then K_FULL[NK], K_EMPTY[NK], V_FULL[NV], V_EMPTY[NV]
+  BAR_DRAIN = 23,        // final commit of the MMA threads
+  BAR_ORDER = 24,        // +i, issue turn of MMA issuer i (forced ordering of the two Q tiles)
+  BAR_FIXED = 26         // then K_FULL[NK], K_EMPTY[NK], V_FULL[NV], V_EMPTY[NV]
 };
 
 // Consumers of a scheduler slot: the two MMA lanes, 2 softmax warpgroups, the
@@ -412,21 +413,27 @@ __device__ __forceinline__ void issue_s(const Ctx& c, int i, uint32_t kstage) {
   }
 }
 
-template <class T>
+// O_i += P_i V for keys [64*HALF, 64*HALF + 64) of the tile.
+template <class T, int HALF>
 __device__ __forceinline__ void issue_pv(const Ctx& c, int i, uint32_t vstage, bool accumulate) {
   constexpr uint32_t HI = ptx::sdesc_hi_sw128(1024);
   const uint32_t d = c.tmem + T::tm_o(i);
   const uint32_t a = c.tmem + T::tm_s(i);
   const uint32_t va = ptx::sdesc_lo(ptx::opaque(c.sbase + T::OFF_V + vstage * T::V_STAGE_BYTES), T::CHUNK_BYTES);
 #pragma unroll
-  for (int kk = 0; kk < kBlockN / 16; ++kk)
+  for (int kk = 4 * HALF; kk < 4 * HALF + 4; ++kk)
     ptx::mma_bf16_ts_lo<HI, T::IDESC_PV>(d, a + kk * 8, va + kk * (2048 >> 4), (accumulate || kk > 0) ? 1u : 0u);
 }
 
-// One MMA-issuing warp per Q tile (warp 12 for tile 0, warp 13 for tile 1):
-// each issues S_i = Q_i K_j^T and O_i += P_i V_j for its own tile, so the
-// waits of one tile overlap the other tile's MMAs on the tensor core. K, V and
-// Q stages are released by one commit from each issuer.
+// One MMA-issuing warp per Q tile (warp 12 for tile 0, warp 13 for tile 1).
+// Per K/V step g each issues one group, O_i += P_i V_{g-1} then S_i = Q_i K_g^T
+// (P_i V first: S_i overwrites the columns holding P_i). The groups of the
+// two issuers strictly alternate through a turn token (the forced-ordering
+// barriers of the layout page): the tensor core runs tile 0's group while
+// tile 1's softmax runs and the other way round. Tile 0, which visits at most
+// as many K/V tiles as tile 1, pads with empty groups so that the
+// alternation never has to wait for the next work tile. K, V and Q stages are
+// released by one commit from each issuer.
 template <class T, bool CAUSAL>
 __device__ void role_mma(const Tc05Params& P, const Ctx& c, const int i) {
   const bool leader = (threadIdx.x & 31) == 0;
@@ -434,7 +441,9 @@ __device__ void role_mma(const Tc05Params& P, const Ctx& c, const int i) {
   Ring<2> sched;
   Ring<T::NK> kr;   // stage of the next K tile
   Ring<T::NV> vr;   // stage of the next V tile
-  uint32_t q_full_phase = 0, p_phase = 0, ofree_phase = 0;
+  uint32_t q_full_phase = 0, p_phase = 0, ofree_phase = 0, order_phase = 0;
+  // Issuer 0 takes the first turn: its first wait passes on the fresh barrier.
+  const uint32_t order_flip = i == 0 ? 1u : 0u;
   bool aborted = false;
 #define AF_WAIT(id, par)                    \
   if (!wait_warp(c, (id), (par), role)) {   \
@@ -457,58 +466,58 @@ __device__ void role_mma(const Tc05Params& P, const Ctx& c, const int i) {
     }
     AF_WAIT(BAR_Q_FULL + i, q_full_phase);
     q_full_phase ^= 1u;
-    // S_i(0)
-    AF_WAIT(T::BAR_K_FULL + kr.idx, kr.phase);
-    ptx::tc_fence_after();
-    if (leader) {
-      issue_s<T>(c, i, kr.idx);
-      ptx::mma_commit(c.bar(BAR_S_FULL + i));
-      ptx::mma_commit(c.bar(T::BAR_K_EMPTY + kr.idx));
-      if (n == 1) ptx::mma_commit(c.bar(BAR_Q_EMPTY));
-    }
-    __syncwarp();
-    kr.next();
-    for (int j = 1; j <= n; ++j) {
-      // O_i += P_i V_{j-1}
-      AF_WAIT(BAR_P_FULL + i, p_phase);
-      p_phase ^= 1u;
-      if (j == 1) {
+    for (int grp = 0; grp <= n1; ++grp) {
+      const bool has_pv = grp >= 1 && grp <= n;
+      const bool has_s = grp < n;
+      // Operands that are usually ready first; the softmax's P last.
+      if (has_pv && grp == 1) {
         AF_WAIT(BAR_O_FREE + i, ofree_phase ^ 1u);
         ofree_phase ^= 1u;
       }
-      AF_WAIT(T::BAR_V_FULL + vr.idx, vr.phase);
-      ptx::tc_fence_after();
-      if (leader) {
-        issue_pv<T>(c, i, vr.idx, j > 1);
-        ptx::mma_commit(c.bar(T::BAR_V_EMPTY + vr.idx));
-        if (j == n) ptx::mma_commit(c.bar(BAR_O_FINAL + i));
+      if (has_pv) AF_WAIT(T::BAR_V_FULL + vr.idx, vr.phase);
+      if (has_s) AF_WAIT(T::BAR_K_FULL + kr.idx, kr.phase);
+      AF_WAIT(BAR_ORDER + i, order_phase ^ order_flip);
+      order_phase ^= 1u;
+      if (has_pv) {
+        AF_WAIT(BAR_P_LO + i, p_phase);
+        ptx::tc_fence_after();
+        if (leader) issue_pv<T, 0>(c, i, vr.idx, grp > 1);
+        __syncwarp();
+        AF_WAIT(BAR_P_HI + i, p_phase);
+        p_phase ^= 1u;
+        ptx::tc_fence_after();
+        if (leader) {
+          issue_pv<T, 1>(c, i, vr.idx, true);
+          ptx::mma_commit(c.bar(T::BAR_V_EMPTY + vr.idx));
+          if (grp == n) ptx::mma_commit(c.bar(BAR_O_FINAL + i));
+        }
+        __syncwarp();
+        vr.next();
       }
-      __syncwarp();
-      vr.next();
-      if (j < n) {  // S_i = Q_i K_j^T
-        AF_WAIT(T::BAR_K_FULL + kr.idx, kr.phase);
+      if (has_s) {
         ptx::tc_fence_after();
         if (leader) {
           issue_s<T>(c, i, kr.idx);
           ptx::mma_commit(c.bar(BAR_S_FULL + i));
           ptx::mma_commit(c.bar(T::BAR_K_EMPTY + kr.idx));
-          if (j == n - 1) ptx::mma_commit(c.bar(BAR_Q_EMPTY));
+          if (grp == n - 1) ptx::mma_commit(c.bar(BAR_Q_EMPTY));
         }
         __syncwarp();
         kr.next();
       }
-    }
-    if (aborted) break;
-    // K/V tiles only the other Q tile visits: release this issuer's share.
-    for (int j = n; j < n1; ++j) {
-      AF_WAIT(T::BAR_K_FULL + kr.idx, kr.phase);
-      if (leader) ptx::mma_commit(c.bar(T::BAR_K_EMPTY + kr.idx));
+      if (leader) ptx::mbar_arrive(c.bar(BAR_ORDER + (i ^ 1)));   // the other issuer's turn
       __syncwarp();
-      kr.next();
-      AF_WAIT(T::BAR_V_FULL + vr.idx, vr.phase);
-      if (leader) ptx::mma_commit(c.bar(T::BAR_V_EMPTY + vr.idx));
-      __syncwarp();
-      vr.next();
+      if (!has_pv && !has_s) {
+        // A K/V tile only the other Q tile visits: release this issuer's share.
+        AF_WAIT(T::BAR_K_FULL + kr.idx, kr.phase);
+        if (leader) ptx::mma_commit(c.bar(T::BAR_K_EMPTY + kr.idx));
+        __syncwarp();
+        kr.next();
+        AF_WAIT(T::BAR_V_FULL + vr.idx, vr.phase);
+        if (leader) ptx::mma_commit(c.bar(T::BAR_V_EMPTY + vr.idx));
+        __syncwarp();
+        vr.next();
+      }
     }
     if (aborted) break;
   }
@@ -625,40 +634,44 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
       const uint64_t c2 = ptx::f2_pack(c_row, c_row);
       const uint64_t n2 = ptx::f2_pack(-m_use, -m_use);
       uint64_t acc0 = 0, acc1 = 0;   // (+0.0f, +0.0f) pairs
-      uint32_t pk[64];
 #pragma unroll
-      for (int e = 0; e < 64; ++e) {
-        float x0, x1;
-        ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(sv[2 * e], sv[2 * e + 1]), c2, n2), x0, x1);
-        const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
-        if (e & 1) acc1 = ptx::f2_add(acc1, ptx::f2_pack(p0, p1));
-        else acc0 = ptx::f2_add(acc0, ptx::f2_pack(p0, p1));
-        pk[e] = ptx::pack_bf16(p0, p1);
+      for (int half = 0; half < 2; ++half) {
+        // P for keys [64*half, 64*half + 64) -> 32 packed bf16 pairs.
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int el = 64 * half + 2 * e;
+          float x0, x1;
+          ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(sv[el], sv[el + 1]), c2, n2), x0, x1);
+          const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+          if (e & 1) acc1 = ptx::f2_add(acc1, ptx::f2_pack(p0, p1));
+          else acc0 = ptx::f2_add(acc0, ptx::f2_pack(p0, p1));
+          pk[e] = ptx::pack_bf16(p0, p1);
+        }
+        ptx::tmem_st32(tS + 32 * half, pk);
+        if (half == 0 && __any_sync(kFull, alpha != 1.f)) {
+          // Correction: the running max moved (rare with the 2^8 headroom), so
+          // rescale this warp's rows of O_i before the next P V accumulates
+          // into it. P_i(j-1) V was complete when S_i(j) arrived (same issuer,
+          // in order).
+#pragma unroll 1
+          for (int q = 0; q < T::DV / 32; ++q) {
+            uint32_t r[32];
+            ptx::tmem_ld32(tO + 32 * q, r);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            ptx::tmem_st32(tO + 32 * q, r);
+          }
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(c.bar((half == 0 ? BAR_P_LO : BAR_P_HI) + i));
       }
       float s0, s1, s2, s3;
       ptx::f2_unpack(acc0, s0, s1);
       ptx::f2_unpack(acc1, s2, s3);
       l = l * alpha + ((s0 + s1) + (s2 + s3));
-      ptx::tmem_st32(tS, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-      ptx::tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
-      ptx::tmem_wait_st();
-      // Correction: the running max moved (rare with the 2^8 headroom), so
-      // rescale this warp's rows of O_i before the next P V accumulates into
-      // it. P_i(j-1) V was complete when S_i(j) arrived (same issuer, in order).
-      if (__any_sync(kFull, alpha != 1.f)) {
-#pragma unroll 1
-        for (int q = 0; q < T::DV / 32; ++q) {
-          uint32_t r[32];
-          ptx::tmem_ld32(tO + 32 * q, r);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-          ptx::tmem_st32(tO + 32 * q, r);
-        }
-        ptx::tmem_wait_st();
-      }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(c.bar(BAR_P_FULL + i));
       m = m_use;
     }
     // Row statistics: LSE (natural log) here, 1/l to the epilogue.
@@ -763,9 +776,10 @@ __global__ void __launch_bounds__(512, 1) fa_tc05_kernel(const __grid_constant__
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(c.bar(BAR_Q_FULL + i), 1);
       ptx::mbar_init(c.bar(BAR_S_FULL + i), 1);
-      ptx::mbar_init(c.bar(BAR_P_FULL + i), 128);
+      ptx::mbar_init(c.bar(BAR_P_LO + i), 128);
       ptx::mbar_init(c.bar(BAR_STATS + i), 128);
-      ptx::mbar_init(c.bar(BAR_UNUSED + i), 1);
+      ptx::mbar_init(c.bar(BAR_P_HI + i), 128);
+      ptx::mbar_init(c.bar(BAR_ORDER + i), 1);
       ptx::mbar_init(c.bar(BAR_O_FINAL + i), 1);
       ptx::mbar_init(c.bar(BAR_O_FREE + i), 128);
       ptx::mbar_init(c.bar(BAR_STATS_FREE + i), 128);
