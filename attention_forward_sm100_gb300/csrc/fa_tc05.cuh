@@ -162,6 +162,23 @@ __device__ __forceinline__ bool wait_warp(const Ctx& c, int id, uint32_t parity,
   }
 }
 
+// Bounded wait of a single thread (the MMA issuers).
+__device__ __forceinline__ bool wait_one(const Ctx& c, int id, uint32_t parity, int role) {
+  const uint32_t bar = c.bar(id);
+  if (ptx::mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0u) {
+      if (*c.abort_flag != 0) return false;
+      if (ptx::globaltimer() - t0 > kTimeoutNs) {
+        raise_error(c, role, id);
+        return false;
+      }
+    }
+  }
+}
+
 // Bounded wait of one thread that ignores the abort flag (drain paths).
 __device__ __forceinline__ bool wait_drain(const Ctx& c, int id, uint32_t parity) {
   const uint32_t bar = c.bar(id);
@@ -436,7 +453,7 @@ __device__ __forceinline__ void issue_pv(const Ctx& c, int i, uint32_t vstage, b
 // released by one commit from each issuer.
 template <class T, bool CAUSAL>
 __device__ void role_mma(const Tc05Params& P, const Ctx& c, const int i) {
-  const bool leader = (threadIdx.x & 31) == 0;
+  // Runs on lane 0 of warp 12 + i only: one thread issues, waits and commits.
   const int role = kRoleMma;
   Ring<2> sched;
   Ring<T::NK> kr;   // stage of the next K tile
@@ -445,15 +462,15 @@ __device__ void role_mma(const Tc05Params& P, const Ctx& c, const int i) {
   // Issuer 0 takes the first turn: its first wait passes on the fresh barrier.
   const uint32_t order_flip = i == 0 ? 1u : 0u;
   bool aborted = false;
-#define AF_WAIT(id, par)                    \
-  if (!wait_warp(c, (id), (par), role)) {   \
-    aborted = true;                         \
-    break;                                  \
+#define AF_WAIT(id, par)                   \
+  if (!wait_one(c, (id), (par), role)) {   \
+    aborted = true;                        \
+    break;                                 \
   }
   while (true) {
-    if (!wait_warp(c, BAR_SCHED_FULL + sched.idx, sched.phase, role)) { aborted = true; break; }
+    if (!wait_one(c, BAR_SCHED_FULL + sched.idx, sched.phase, role)) { aborted = true; break; }
     const SchedSlot s = read_slot(c, sched.idx, T::OFF_SCHED);
-    if (leader) ptx::mbar_arrive(c.bar(BAR_SCHED_EMPTY + sched.idx));
+    ptx::mbar_arrive(c.bar(BAR_SCHED_EMPTY + sched.idx));
     sched.next();
     if (!s.valid) break;
     const Geo g = tile_geo<CAUSAL>(s);
@@ -469,53 +486,45 @@ __device__ void role_mma(const Tc05Params& P, const Ctx& c, const int i) {
     for (int grp = 0; grp <= n1; ++grp) {
       const bool has_pv = grp >= 1 && grp <= n;
       const bool has_s = grp < n;
-      // Operands that are usually ready first; the softmax's P last.
-      if (has_pv && grp == 1) {
-        AF_WAIT(BAR_O_FREE + i, ofree_phase ^ 1u);
-        ofree_phase ^= 1u;
+      // Everything but the second half of P is waited for before taking the
+      // turn, so the turn is spent issuing.
+      if (has_pv) {
+        if (grp == 1) {
+          AF_WAIT(BAR_O_FREE + i, ofree_phase ^ 1u);
+          ofree_phase ^= 1u;
+        }
+        AF_WAIT(T::BAR_V_FULL + vr.idx, vr.phase);
+        AF_WAIT(BAR_P_LO + i, p_phase);
       }
-      if (has_pv) AF_WAIT(T::BAR_V_FULL + vr.idx, vr.phase);
       if (has_s) AF_WAIT(T::BAR_K_FULL + kr.idx, kr.phase);
       AF_WAIT(BAR_ORDER + i, order_phase ^ order_flip);
       order_phase ^= 1u;
+      ptx::tc_fence_after();
       if (has_pv) {
-        AF_WAIT(BAR_P_LO + i, p_phase);
-        ptx::tc_fence_after();
-        if (leader) issue_pv<T, 0>(c, i, vr.idx, grp > 1);
-        __syncwarp();
+        issue_pv<T, 0>(c, i, vr.idx, grp > 1);
         AF_WAIT(BAR_P_HI + i, p_phase);
         p_phase ^= 1u;
         ptx::tc_fence_after();
-        if (leader) {
-          issue_pv<T, 1>(c, i, vr.idx, true);
-          ptx::mma_commit(c.bar(T::BAR_V_EMPTY + vr.idx));
-          if (grp == n) ptx::mma_commit(c.bar(BAR_O_FINAL + i));
-        }
-        __syncwarp();
+        issue_pv<T, 1>(c, i, vr.idx, true);
+        ptx::mma_commit(c.bar(T::BAR_V_EMPTY + vr.idx));
+        if (grp == n) ptx::mma_commit(c.bar(BAR_O_FINAL + i));
         vr.next();
       }
       if (has_s) {
-        ptx::tc_fence_after();
-        if (leader) {
-          issue_s<T>(c, i, kr.idx);
-          ptx::mma_commit(c.bar(BAR_S_FULL + i));
-          ptx::mma_commit(c.bar(T::BAR_K_EMPTY + kr.idx));
-          if (grp == n - 1) ptx::mma_commit(c.bar(BAR_Q_EMPTY));
-        }
-        __syncwarp();
+        issue_s<T>(c, i, kr.idx);
+        ptx::mma_commit(c.bar(BAR_S_FULL + i));
+        ptx::mma_commit(c.bar(T::BAR_K_EMPTY + kr.idx));
+        if (grp == n - 1) ptx::mma_commit(c.bar(BAR_Q_EMPTY));
         kr.next();
       }
-      if (leader) ptx::mbar_arrive(c.bar(BAR_ORDER + (i ^ 1)));   // the other issuer's turn
-      __syncwarp();
+      ptx::mbar_arrive(c.bar(BAR_ORDER + (i ^ 1)));   // the other issuer's turn
       if (!has_pv && !has_s) {
         // A K/V tile only the other Q tile visits: release this issuer's share.
         AF_WAIT(T::BAR_K_FULL + kr.idx, kr.phase);
-        if (leader) ptx::mma_commit(c.bar(T::BAR_K_EMPTY + kr.idx));
-        __syncwarp();
+        ptx::mma_commit(c.bar(T::BAR_K_EMPTY + kr.idx));
         kr.next();
         AF_WAIT(T::BAR_V_FULL + vr.idx, vr.phase);
-        if (leader) ptx::mma_commit(c.bar(T::BAR_V_EMPTY + vr.idx));
-        __syncwarp();
+        ptx::mma_commit(c.bar(T::BAR_V_EMPTY + vr.idx));
         vr.next();
       }
     }
@@ -524,12 +533,9 @@ __device__ void role_mma(const Tc05Params& P, const Ctx& c, const int i) {
 #undef AF_WAIT
   // Drain: the arrive of this commit follows every MMA and commit this thread
   // issued (both issuers commit; the phase completes after both).
-  if (leader) {
-    ptx::mma_commit(c.bar(BAR_DRAIN));
-    wait_drain(c, BAR_DRAIN, 0);
-  }
+  ptx::mma_commit(c.bar(BAR_DRAIN));
+  wait_drain(c, BAR_DRAIN, 0);
   (void)aborted;
-  __syncwarp();
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -829,7 +835,10 @@ __global__ void __launch_bounds__(512, 1) fa_tc05_kernel(const __grid_constant__
     role_correction<T, CAUSAL>(P, c);
   } else {
     setmaxnreg_dec<T::REG_MISC>();
-    if (warp == 12 || warp == 13) role_mma<T, CAUSAL>(P, c, warp - 12);
+    if (warp == 12 || warp == 13) {
+      if (lane == 0) role_mma<T, CAUSAL>(P, c, warp - 12);
+      __syncwarp();
+    }
     else if (warp == 14) role_load_qk<T, CAUSAL>(P, c);
     else role_load_v<T, CAUSAL>(P, c);
   }
