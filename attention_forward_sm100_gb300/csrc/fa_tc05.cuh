@@ -51,7 +51,7 @@ enum Role : int { kRoleSoftmax0 = 0, kRoleSoftmax1 = 1, kRoleCorrection = 2, kRo
 
 enum BarId : int {
   BAR_Q_FULL = 0,        // +i, TMA transaction barrier of Q tile i
-  BAR_Q_EMPTY = 2,       // last S MMA of a work tile done: Q region free
+  BAR_Q_EMPTY = 2,       // last S MMA of Q tile 0 done: its Q region is free (tile 1: BAR_Q_EMPTY1)
   BAR_S_FULL = 3,        // +i, S_i = Q_i K^T complete
   BAR_P_LO = 5,          // +i, first half of P_i (keys 0..63) in tensor memory (128 arrivals)
   BAR_STATS = 7,         // +i, final 1/l of Q tile i in shared memory (128 arrivals)
@@ -64,7 +64,8 @@ enum BarId : int {
   BAR_SCHED_EMPTY = 21,  // +slot
   BAR_DRAIN = 23,        // final commit of the MMA threads
   BAR_ORDER = 24,        // +i, issue turn of MMA issuer i (forced ordering of the two Q tiles)
-  BAR_FIXED = 26         // then K_FULL[NK], K_EMPTY[NK], V_FULL[NV], V_EMPTY[NV]
+  BAR_Q_EMPTY1 = 26,     // last S MMA of Q tile 1 done
+  BAR_FIXED = 27         // then K_FULL[NK], K_EMPTY[NK], V_FULL[NV], V_EMPTY[NV]
 };
 
 // Consumers of a scheduler slot: the two MMA lanes, 2 softmax warpgroups, the
@@ -116,6 +117,8 @@ struct Tc05Traits {
   static constexpr uint32_t IDESC_S =
       FP8 ? ptx::idesc_f32acc(0, 0, false, false, 128, 128) : ptx::idesc_f32acc(1, 1, false, false, 128, 128);
   static constexpr uint32_t IDESC_PV = ptx::idesc_f32acc(1, 1, false, true, 128, DV);
+  // MMA instructions of one S = Q K^T (K = 16 per bf16 instruction, 32 per fp8).
+  static constexpr int S_INSTR = FP8 ? DQK / 32 : (DQK + DR) / 16;
 
   // Register split (setmaxnreg) of a 512-thread CTA launched with 128 registers per thread.
   static constexpr int REG_SOFTMAX = 184, REG_CORR = 80, REG_MISC = 64;
@@ -135,6 +138,7 @@ struct Ctx {
   uint32_t* ws;
   int bar_off;
   __device__ __forceinline__ uint32_t bar(int i) const { return sbase + bar_off + 8u * (uint32_t)i; }
+  __device__ __forceinline__ static int q_empty_id(int i) { return i == 0 ? BAR_Q_EMPTY : BAR_Q_EMPTY1; }
 };
 
 __device__ __forceinline__ void raise_error(const Ctx& c, int role, int id) {
@@ -177,6 +181,16 @@ __device__ __forceinline__ bool wait_one(const Ctx& c, int id, uint32_t parity, 
       }
     }
   }
+}
+
+// Same, polling without suspending for a while first (the issue turn, whose
+// hand-off latency is on the tensor core's critical path).
+__device__ __forceinline__ bool wait_one_spin(const Ctx& c, int id, uint32_t parity, int role) {
+  const uint32_t bar = c.bar(id);
+#pragma unroll 1
+  for (int k = 0; k < 512; ++k)
+    if (ptx::mbar_test_wait(bar, parity)) return true;
+  return wait_one(c, id, parity, role);
 }
 
 // Bounded wait of one thread that ignores the abort flag (drain paths).
@@ -285,7 +299,8 @@ __device__ void role_load_qk(const Tc05Params& P, const Ctx& c) {
   uint32_t q_empty_phase = 0;
   uint32_t k_fill_parity[T::NK];
   bool k_used[T::NK];
-  bool q_used = false;
+  bool q_loaded[2] = {false, false};
+  uint32_t q_fill_parity = 0;
 #pragma unroll
   for (int s = 0; s < T::NK; ++s) { k_fill_parity[s] = 0; k_used[s] = false; }
   Cursor cur;
@@ -308,23 +323,23 @@ __device__ void role_load_qk(const Tc05Params& P, const Ctx& c) {
     if (n1 > 0) {
       const int hk = s.h / P.group;
       const int qb = P.packed ? 0 : s.b;
+      auto load_q = [&](int i) {
+        const uint32_t bar = c.bar(BAR_Q_FULL + i);
+        const uint32_t dst = c.sbase + T::OFF_Q + i * T::Q_TILE_BYTES;
+        const int row = s.q_start + g.q0 + kBlockM * i;
+        ptx::mbar_expect_tx(bar, T::Q_TILE_BYTES);
+#pragma unroll
+        for (int ch = 0; ch < T::QK_CHUNKS; ++ch)
+          ptx::tma_load_4d(dst + ch * T::CHUNK_BYTES, &P.tm_q, bar, ch * T::QK_CHUNK_ELEMS, s.h, row, qb);
+        if (T::DR > 0) ptx::tma_load_4d(dst + T::QK_CHUNKS * T::CHUNK_BYTES, &P.tm_qr, bar, 0, s.h, row, qb);
+      };
+      // Q tile 0, K_0, then Q tile 1: each Q region is refilled as soon as
+      // its own last S MMA of the previous work tile is done.
       if (!wait_warp(c, BAR_Q_EMPTY, q_empty_phase ^ 1u, kRoleLoadQK)) { aborted = true; break; }
-      q_empty_phase ^= 1u;
-      if (lane == 0) {
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const uint32_t bar = c.bar(BAR_Q_FULL + i);
-          const uint32_t dst = c.sbase + T::OFF_Q + i * T::Q_TILE_BYTES;
-          const int row = s.q_start + g.q0 + kBlockM * i;
-          ptx::mbar_expect_tx(bar, T::Q_TILE_BYTES);
-#pragma unroll
-          for (int ch = 0; ch < T::QK_CHUNKS; ++ch)
-            ptx::tma_load_4d(dst + ch * T::CHUNK_BYTES, &P.tm_q, bar, ch * T::QK_CHUNK_ELEMS, s.h, row, qb);
-          if (T::DR > 0)
-            ptx::tma_load_4d(dst + T::QK_CHUNKS * T::CHUNK_BYTES, &P.tm_qr, bar, 0, s.h, row, qb);
-        }
-      }
-      q_used = true;
+      if (lane == 0) load_q(0);
+      q_fill_parity = q_empty_phase;   // parity of the Q_FULL phases these loads complete
+      q_loaded[0] = true;
+      q_loaded[1] = false;
       for (int j = 0; j < n1; ++j) {
         if (!wait_warp(c, T::BAR_K_EMPTY + kr.idx, kr.phase ^ 1u, kRoleLoadQK)) { aborted = true; break; }
         if (lane == 0) {
@@ -340,6 +355,12 @@ __device__ void role_load_qk(const Tc05Params& P, const Ctx& c) {
         k_fill_parity[kr.idx] = kr.phase;
         k_used[kr.idx] = true;
         kr.next();
+        if (j == 0) {
+          if (!wait_warp(c, BAR_Q_EMPTY1, q_empty_phase ^ 1u, kRoleLoadQK)) { aborted = true; break; }
+          if (lane == 0) load_q(1);
+          q_loaded[1] = true;
+          q_empty_phase ^= 1u;
+        }
       }
       if (aborted) break;
     }
@@ -353,10 +374,9 @@ __device__ void role_load_qk(const Tc05Params& P, const Ctx& c) {
 #pragma unroll
     for (int s = 0; s < T::NK; ++s)
       if (k_used[s]) wait_drain(c, T::BAR_K_FULL + s, k_fill_parity[s]);
-    if (q_used) {
-      wait_drain(c, BAR_Q_FULL + 0, (q_empty_phase ^ 1u));
-      wait_drain(c, BAR_Q_FULL + 1, (q_empty_phase ^ 1u));
-    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+      if (q_loaded[i]) wait_drain(c, BAR_Q_FULL + i, q_fill_parity);
   }
   __syncwarp();
 }
@@ -406,25 +426,23 @@ __device__ void role_load_v(const Tc05Params& P, const Ctx& c) {
 }
 
 // ---------------------------------------------------------------------------------------------
-template <class T>
+// S_i = Q_i K^T, MMA instructions [B, E) of the K loop (nope part first,
+// then the shared rope part).
+template <class T, int B, int E>
 __device__ __forceinline__ void issue_s(const Ctx& c, int i, uint32_t kstage) {
   constexpr uint32_t HI = ptx::sdesc_hi_sw128(1024);
   const uint32_t d = c.tmem + T::tm_s(i);
   const uint32_t qa = ptx::sdesc_lo(ptx::opaque(c.sbase + T::OFF_Q + i * T::Q_TILE_BYTES), 16);
   const uint32_t ka = ptx::sdesc_lo(ptx::opaque(c.sbase + T::OFF_K + kstage * T::K_STAGE_BYTES), 16);
-  if (T::FP8) {
 #pragma unroll
-    for (int kk = 0; kk < T::DQK / 32; ++kk)
+  for (int kk = B; kk < E; ++kk) {
+    if (T::FP8) {
       ptx::mma_fp8_ss_lo<HI, HI, T::IDESC_S>(d, qa + kk * 2, ka + kk * 2, kk > 0);
-  } else {
-#pragma unroll
-    for (int kk = 0; kk < T::DQK / 16; ++kk) {
+    } else if (kk < T::DQK / 16) {
       const uint32_t off = ((kk >> 2) * T::CHUNK_BYTES + (kk & 3) * 32) >> 4;
       ptx::mma_bf16_ss_lo<HI, HI, T::IDESC_S>(d, qa + off, ka + off, kk > 0);
-    }
-#pragma unroll
-    for (int kk = 0; kk < T::DR / 16; ++kk) {
-      const uint32_t off = (T::QK_CHUNKS * T::CHUNK_BYTES + kk * 32) >> 4;
+    } else {
+      const uint32_t off = (T::QK_CHUNKS * T::CHUNK_BYTES + (kk - T::DQK / 16) * 32) >> 4;
       ptx::mma_bf16_ss_lo<HI, HI, T::IDESC_S>(d, qa + off, ka + off, 1u);
     }
   }
@@ -497,7 +515,7 @@ __device__ void role_mma(const Tc05Params& P, const Ctx& c, const int i) {
         AF_WAIT(BAR_P_LO + i, p_phase);
       }
       if (has_s) AF_WAIT(T::BAR_K_FULL + kr.idx, kr.phase);
-      AF_WAIT(BAR_ORDER + i, order_phase ^ order_flip);
+      if (!wait_one_spin(c, BAR_ORDER + i, order_phase ^ order_flip, role)) { aborted = true; break; }
       order_phase ^= 1u;
       ptx::tc_fence_after();
       if (has_pv) {
@@ -511,13 +529,19 @@ __device__ void role_mma(const Tc05Params& P, const Ctx& c, const int i) {
         vr.next();
       }
       if (has_s) {
-        issue_s<T>(c, i, kr.idx);
+        // Hand the turn over before the last two instructions: they are queued
+        // ahead of anything the other issuer sends, and its wake-up overlaps
+        // their execution.
+        issue_s<T, 0, T::S_INSTR - 2>(c, i, kr.idx);
+        ptx::mbar_arrive(c.bar(BAR_ORDER + (i ^ 1)));
+        issue_s<T, T::S_INSTR - 2, T::S_INSTR>(c, i, kr.idx);
         ptx::mma_commit(c.bar(BAR_S_FULL + i));
         ptx::mma_commit(c.bar(T::BAR_K_EMPTY + kr.idx));
-        if (grp == n - 1) ptx::mma_commit(c.bar(BAR_Q_EMPTY));
+        if (grp == n - 1) ptx::mma_commit(c.bar(Ctx::q_empty_id(i)));
         kr.next();
+      } else {
+        ptx::mbar_arrive(c.bar(BAR_ORDER + (i ^ 1)));   // the other issuer's turn
       }
-      ptx::mbar_arrive(c.bar(BAR_ORDER + (i ^ 1)));   // the other issuer's turn
       if (!has_pv && !has_s) {
         // A K/V tile only the other Q tile visits: release this issuer's share.
         AF_WAIT(T::BAR_K_FULL + kr.idx, kr.phase);
@@ -793,7 +817,8 @@ __global__ void __launch_bounds__(512, 1) fa_tc05_kernel(const __grid_constant__
       ptx::mbar_init(c.bar(BAR_SCHED_FULL + i), 1);
       ptx::mbar_init(c.bar(BAR_SCHED_EMPTY + i), kSchedConsumers);
     }
-    ptx::mbar_init(c.bar(BAR_Q_EMPTY), 2);
+    ptx::mbar_init(c.bar(BAR_Q_EMPTY), 1);
+    ptx::mbar_init(c.bar(BAR_Q_EMPTY1), 1);
     ptx::mbar_init(c.bar(BAR_DRAIN), 2);
 #pragma unroll
     for (int s = 0; s < T::NK; ++s) {

@@ -109,7 +109,7 @@ class ClockSampler:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=self.file, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
 
@@ -138,7 +138,8 @@ class ClockSampler:
                 if val.lower() in ("active", "1"):
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "window": "timed steps plus ~1 s of the same steps right after them"}
 
 
 def cpu_baseline(spec, inputs, seconds):
@@ -302,6 +303,13 @@ def main():
         step()
         ev[i + 1].record(stream)
     torch.cuda.synchronize(dev)
+    # The timed steps last milliseconds, nvidia-smi samples every 100 ms: keep
+    # the same load running right after them until a second of samples exists.
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < 1.0:
+        for _ in range(64):
+            step()
+        torch.cuda.synchronize(dev)
     barrier(world)
     clk = clocks.stop()
     pkg.check(device=dev)
