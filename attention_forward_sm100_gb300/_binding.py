@@ -45,6 +45,7 @@ class Params(ctypes.Structure):
         ("q_stride", ctypes.c_int64 * 3), ("k_stride", ctypes.c_int64 * 3), ("v_stride", ctypes.c_int64 * 3),
         ("o_stride", ctypes.c_int64 * 3), ("q_rope_stride", ctypes.c_int64 * 3),
         ("k_rope_stride", ctypes.c_int64 * 2),
+        ("fault_injection", ctypes.c_int32),
     ]
 
 

@@ -37,6 +37,8 @@ attn_status validate(const attn_fwd_params* p) {
     return fail(ATTN_ERR_INVALID_ARG, "unknown qk_dtype %d", p->qk_dtype);
   if (p->backend != ATTN_BACKEND_TCGEN05 && p->backend != ATTN_BACKEND_SIMPLE)
     return fail(ATTN_ERR_INVALID_ARG, "unknown backend %d", p->backend);
+  if (p->fault_injection != 0 && p->fault_injection != 1)
+    return fail(ATTN_ERR_INVALID_ARG, "unknown fault_injection %d", p->fault_injection);
   if (p->batch < 0 || p->seqlen_q < 0 || p->seqlen_k < 0 || p->total_q < 0 || p->total_k < 0)
     return fail(ATTN_ERR_INVALID_ARG, "negative size");
   if (p->num_heads_q <= 0 || p->num_heads_kv <= 0)
@@ -236,6 +238,8 @@ attn_status launch_tc05(const attn_fwd_params* p, cudaStream_t stream) {
   prm.total_q = packed ? p->total_q : 0;
   prm.total_k = packed ? p->total_k : 0;
   prm.scale_log2 = p->softmax_scale * 1.4426950408889634f;
+  prm.withhold_v = p->fault_injection == 1 ? 1 : 0;
+  prm.timeout_ns = prm.withhold_v ? 200000000ull : 2000000000ull;
   int64_t bound = work_tiles_bound(p);
   if (bound <= 0) return ATTN_OK;
   const int grid = (int)(bound < sm_count_cached() ? bound : sm_count_cached());

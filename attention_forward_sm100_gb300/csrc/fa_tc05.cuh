@@ -43,7 +43,6 @@
 namespace af {
 
 constexpr uint32_t kFull = 0xffffffffu;
-constexpr uint64_t kTimeoutNs = 2000000000ull;   // 2 s per wait
 constexpr uint64_t kDrainTimeoutNs = 100000000ull;
 
 enum Role : int { kRoleSoftmax0 = 0, kRoleSoftmax1 = 1, kRoleCorrection = 2, kRoleMma = 3, kRoleLoadQK = 4,
@@ -119,6 +118,9 @@ struct Tc05Traits {
   static constexpr uint32_t IDESC_PV = ptx::idesc_f32acc(1, 1, false, true, 128, DV);
   // MMA instructions of one S = Q K^T (K = 16 per bf16 instruction, 32 per fp8).
   static constexpr int S_INSTR = FP8 ? DQK / 32 : (DQK + DR) / 16;
+  // S instructions issued after handing the turn to the other issuer: enough
+  // tensor work (~4 x 73 cycles) to cover the other issuer's wake-up.
+  static constexpr int S_AFTER_HANDOFF = S_INSTR < 4 ? S_INSTR : 4;
 
   // Register split (setmaxnreg) of a 512-thread CTA launched with 128 registers per thread.
   static constexpr int REG_SOFTMAX = 184, REG_CORR = 80, REG_MISC = 64;
@@ -136,6 +138,7 @@ struct Ctx {
   uint32_t tmem;
   volatile int* abort_flag;
   uint32_t* ws;
+  uint64_t timeout_ns;
   int bar_off;
   __device__ __forceinline__ uint32_t bar(int i) const { return sbase + bar_off + 8u * (uint32_t)i; }
   __device__ __forceinline__ static int q_empty_id(int i) { return i == 0 ? BAR_Q_EMPTY : BAR_Q_EMPTY1; }
@@ -157,7 +160,7 @@ __device__ __forceinline__ bool wait_warp(const Ctx& c, int id, uint32_t parity,
     if ((it & 63u) == 0u) {
       if (__any_sync(kFull, *c.abort_flag != 0)) return false;
       const uint64_t now = __shfl_sync(kFull, ptx::globaltimer(), 0);
-      if (now - t0 > kTimeoutNs) {
+      if (now - t0 > c.timeout_ns) {
         if ((threadIdx.x & 31) == 0) raise_error(c, role, id);
         __syncwarp();
         return false;
@@ -175,7 +178,7 @@ __device__ __forceinline__ bool wait_one(const Ctx& c, int id, uint32_t parity, 
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0u) {
       if (*c.abort_flag != 0) return false;
-      if (ptx::globaltimer() - t0 > kTimeoutNs) {
+      if (ptx::globaltimer() - t0 > c.timeout_ns) {
         raise_error(c, role, id);
         return false;
       }
@@ -390,6 +393,7 @@ __device__ void role_load_v(const Tc05Params& P, const Ctx& c) {
   bool v_used[T::NV];
 #pragma unroll
   for (int s = 0; s < T::NV; ++s) { v_fill_parity[s] = 0; v_used[s] = false; }
+  bool first_v = true;
   bool aborted = false;
   while (true) {
     if (!wait_warp(c, BAR_SCHED_FULL + sched.idx, sched.phase, kRoleLoadV)) { aborted = true; break; }
@@ -402,7 +406,11 @@ __device__ void role_load_v(const Tc05Params& P, const Ctx& c) {
     const int vb = P.packed ? 0 : s.b;
     for (int j = 0; j < g.n[1]; ++j) {
       if (!wait_warp(c, T::BAR_V_EMPTY + vr.idx, vr.phase ^ 1u, kRoleLoadV)) { aborted = true; break; }
-      if (lane == 0) {
+      // Fault injection (testing only): block 0 never loads its first V tile,
+      // so the MMA issuer's bounded wait for it runs out.
+      const bool withhold = P.withhold_v && blockIdx.x == 0 && first_v;
+      first_v = false;
+      if (lane == 0 && !withhold) {
         const uint32_t bar = c.bar(T::BAR_V_FULL + vr.idx);
         const uint32_t dst = c.sbase + T::OFF_V + vr.idx * T::V_STAGE_BYTES;
         const int row = s.k_start + kBlockN * j;
@@ -412,7 +420,7 @@ __device__ void role_load_v(const Tc05Params& P, const Ctx& c) {
           ptx::tma_load_4d(dst + ch * T::CHUNK_BYTES, &P.tm_v, bar, ch * 64, hk, row, vb);
       }
       v_fill_parity[vr.idx] = vr.phase;
-      v_used[vr.idx] = true;
+      v_used[vr.idx] = v_used[vr.idx] || !withhold;
       vr.next();
     }
     if (aborted) break;
@@ -529,12 +537,11 @@ __device__ void role_mma(const Tc05Params& P, const Ctx& c, const int i) {
         vr.next();
       }
       if (has_s) {
-        // Hand the turn over before the last two instructions: they are queued
-        // ahead of anything the other issuer sends, and its wake-up overlaps
-        // their execution.
-        issue_s<T, 0, T::S_INSTR - 2>(c, i, kr.idx);
+        // Hand the turn over before the last S_AFTER_HANDOFF instructions, so
+        // the other issuer's wake-up overlaps their execution.
+        issue_s<T, 0, T::S_INSTR - T::S_AFTER_HANDOFF>(c, i, kr.idx);
         ptx::mbar_arrive(c.bar(BAR_ORDER + (i ^ 1)));
-        issue_s<T, T::S_INSTR - 2, T::S_INSTR>(c, i, kr.idx);
+        issue_s<T, T::S_INSTR - T::S_AFTER_HANDOFF, T::S_INSTR>(c, i, kr.idx);
         ptx::mma_commit(c.bar(BAR_S_FULL + i));
         ptx::mma_commit(c.bar(T::BAR_K_EMPTY + kr.idx));
         if (grp == n - 1) ptx::mma_commit(c.bar(Ctx::q_empty_id(i)));
@@ -796,6 +803,7 @@ __global__ void __launch_bounds__(512, 1) fa_tc05_kernel(const __grid_constant__
   c.ws = P.ws;
   c.abort_flag = reinterpret_cast<volatile int*>(smem + T::OFF_ABORT);
   c.bar_off = T::OFF_BAR;
+  c.timeout_ns = P.timeout_ns;
   if (c.sbase & 1023u) {  // the swizzled tiles need a 1024-byte aligned base
     if (threadIdx.x == 0) atomicCAS(&P.ws[kWsErrorCode], 0u, 2u);
     return;

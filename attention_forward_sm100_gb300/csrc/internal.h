@@ -51,6 +51,8 @@ struct Tc05Params {
   int32_t total_q;         // packed: rows of q (LSE and q_scale layout [Hq, Tq])
   int32_t total_k;         // packed: rows of k (k_scale layout [Hkv, Tk])
   float scale_log2;        // softmax_scale * log2(e)
+  uint64_t timeout_ns;     // limit of every device wait
+  int32_t withhold_v;      // testing: block 0 skips its first V tile load
 };
 
 // Kernel variants of the tcgen05 path.

@@ -107,6 +107,11 @@ typedef struct attn_fwd_params {
   int64_t o_stride[3];
   int64_t q_rope_stride[3];
   int64_t k_rope_stride[2]; /* [0] batch, [1] token */
+
+  /* Testing only; leave 0. 1: the first CTA withholds its first V tile, so a
+   * bounded device wait runs out (limit 200 ms instead of 2 s), the kernel
+   * aborts cleanly and attn_fwd_check reports ATTN_ERR_DEVICE_TIMEOUT. */
+  int32_t fault_injection;
 } attn_fwd_params;
 
 /* Query results of attn_fwd_plan (host only; no GPU needed). */
