@@ -169,14 +169,17 @@ __device__ __forceinline__ bool wait_warp(const Ctx& c, int id, uint32_t parity,
   }
 }
 
-// Bounded wait of a single thread (the MMA issuers).
+// Bounded wait of a single thread (the MMA issuers). It polls without ever
+// suspending: a thread suspended in mbarrier.try_wait was seen to resume
+// hundreds of cycles after the phase completed, and every cycle an issuer
+// loses leaves the tensor core idle.
 __device__ __forceinline__ bool wait_one(const Ctx& c, int id, uint32_t parity, int role) {
   const uint32_t bar = c.bar(id);
   if (ptx::mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer();
   for (uint32_t it = 1;; ++it) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0u) {
+    if (ptx::mbar_test_wait(bar, parity)) return true;
+    if ((it & 255u) == 0u) {
       if (*c.abort_flag != 0) return false;
       if (ptx::globaltimer() - t0 > c.timeout_ns) {
         raise_error(c, role, id);
@@ -184,16 +187,6 @@ __device__ __forceinline__ bool wait_one(const Ctx& c, int id, uint32_t parity, 
       }
     }
   }
-}
-
-// Same, polling without suspending for a while first (the issue turn, whose
-// hand-off latency is on the tensor core's critical path).
-__device__ __forceinline__ bool wait_one_spin(const Ctx& c, int id, uint32_t parity, int role) {
-  const uint32_t bar = c.bar(id);
-#pragma unroll 1
-  for (int k = 0; k < 512; ++k)
-    if (ptx::mbar_test_wait(bar, parity)) return true;
-  return wait_one(c, id, parity, role);
 }
 
 // Bounded wait of one thread that ignores the abort flag (drain paths).
@@ -523,7 +516,7 @@ __device__ void role_mma(const Tc05Params& P, const Ctx& c, const int i) {
         AF_WAIT(BAR_P_LO + i, p_phase);
       }
       if (has_s) AF_WAIT(T::BAR_K_FULL + kr.idx, kr.phase);
-      if (!wait_one_spin(c, BAR_ORDER + i, order_phase ^ order_flip, role)) { aborted = true; break; }
+      if (!wait_one(c, BAR_ORDER + i, order_phase ^ order_flip, role)) { aborted = true; break; }
       order_phase ^= 1u;
       ptx::tc_fence_after();
       if (has_pv) {
