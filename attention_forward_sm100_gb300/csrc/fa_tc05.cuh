@@ -505,19 +505,21 @@ __device__ void role_mma(const Tc05Params& P, const Ctx& c, const int i) {
     for (int grp = 0; grp <= n1; ++grp) {
       const bool has_pv = grp >= 1 && grp <= n;
       const bool has_s = grp < n;
-      // Everything but the second half of P is waited for before taking the
-      // turn, so the turn is spent issuing.
+      // Operands that are usually ready first, then the turn, the softmax's
+      // first half of P last: once it lands the issuer goes straight to
+      // issuing (each barrier check costs this thread ~100-200 cycles while
+      // the softmax warps keep tensor and shared memory busy).
       if (has_pv) {
         if (grp == 1) {
           AF_WAIT(BAR_O_FREE + i, ofree_phase ^ 1u);
           ofree_phase ^= 1u;
         }
         AF_WAIT(T::BAR_V_FULL + vr.idx, vr.phase);
-        AF_WAIT(BAR_P_LO + i, p_phase);
       }
       if (has_s) AF_WAIT(T::BAR_K_FULL + kr.idx, kr.phase);
       if (!wait_one(c, BAR_ORDER + i, order_phase ^ order_flip, role)) { aborted = true; break; }
       order_phase ^= 1u;
+      if (has_pv) AF_WAIT(BAR_P_LO + i, p_phase);
       ptx::tc_fence_after();
       if (has_pv) {
         issue_pv<T, 0>(c, i, vr.idx, grp > 1);
