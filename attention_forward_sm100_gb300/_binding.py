@@ -46,17 +46,20 @@ class Params(ctypes.Structure):
         ("o_stride", ctypes.c_int64 * 3), ("q_rope_stride", ctypes.c_int64 * 3),
         ("k_rope_stride", ctypes.c_int64 * 2),
         ("fault_injection", ctypes.c_int32),
+        ("num_splits", ctypes.c_int32),
     ]
 
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [("backend", ctypes.c_int32), ("rows_per_tile", ctypes.c_int32), ("work_tiles", ctypes.c_int64),
                 ("grid", ctypes.c_int32), ("block", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
-                ("k_stages", ctypes.c_int32), ("v_stages", ctypes.c_int32), ("tmem_columns", ctypes.c_int32)]
+                ("k_stages", ctypes.c_int32), ("v_stages", ctypes.c_int32), ("tmem_columns", ctypes.c_int32),
+                ("num_splits", ctypes.c_int32)]
 
 
 class WorkTile(ctypes.Structure):
-    _fields_ = [("batch", ctypes.c_int32), ("head", ctypes.c_int32), ("tile", ctypes.c_int32)]
+    _fields_ = [("batch", ctypes.c_int32), ("head", ctypes.c_int32), ("tile", ctypes.c_int32),
+                ("split", ctypes.c_int32)]
 
 
 _lib = None
@@ -105,15 +108,22 @@ def last_error() -> str:
 _workspaces = {}
 
 
-def default_workspace(device) -> torch.Tensor:
-    """A zero-filled workspace per device (the library keeps it zeroed)."""
+def default_workspace(device, nbytes: int = WORKSPACE_BYTES) -> torch.Tensor:
+    """A zero-filled workspace per device of at least ``nbytes`` (the library
+    keeps its counters zeroed; split-KV partial results need more room, so
+    the cached buffer is replaced by a larger one when a call asks for it)."""
     device = torch.device(device)
     key = (device.type, device.index)
     ws = _workspaces.get(key)
-    if ws is None:
-        ws = torch.zeros(WORKSPACE_BYTES, dtype=torch.uint8, device=device)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, WORKSPACE_BYTES), dtype=torch.uint8, device=device)
         _workspaces[key] = ws
     return ws
+
+
+def workspace_bytes(p: Params) -> int:
+    """attn_fwd_workspace_bytes: the workspace size ``p`` needs."""
+    return int(lib().attn_fwd_workspace_bytes(ctypes.byref(p)))
 
 
 def _ptr(t):
@@ -127,7 +137,7 @@ def _require_cuda(name, t):
 
 def make_params(q, k, v, *, causal, softmax_scale=None, q_rope=None, k_rope=None, q_scale=None, k_scale=None,
                 cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, out=None, lse=None,
-                workspace=None, backend="tcgen05") -> Params:
+                workspace=None, backend="tcgen05", num_splits=0) -> Params:
     """attn_fwd_params for torch tensors (shapes are read, nothing is allocated)."""
     packed = cu_seqlens_q is not None
     p = Params()
@@ -151,6 +161,7 @@ def make_params(q, k, v, *, causal, softmax_scale=None, q_rope=None, k_rope=None
         raise ValueError(f"unsupported q dtype {q.dtype}")
     p.qk_dtype = DTYPES[q.dtype]
     p.backend = BACKENDS[backend]
+    p.num_splits = int(num_splits)
     p.q, p.k, p.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
     p.q_rope, p.k_rope = _ptr(q_rope), _ptr(k_rope)
     p.q_scale, p.k_scale = _ptr(q_scale), _ptr(k_scale)
@@ -178,7 +189,7 @@ def make_params(q, k, v, *, causal, softmax_scale=None, q_rope=None, k_rope=None
 
 def forward(q, k, v, *, causal=False, softmax_scale=None, q_rope=None, k_rope=None, q_scale=None, k_scale=None,
             cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, out=None, lse=None,
-            return_lse=True, workspace=None, backend="tcgen05", stream=None):
+            return_lse=True, workspace=None, backend="tcgen05", stream=None, num_splits=0):
     """Fused attention forward on the GPU; returns (O, LSE).
 
     Fixed length: q [B,Sq,Hq,D], k [B,Sk,Hkv,D], v [B,Sk,Hkv,Dv] -> O
@@ -186,8 +197,10 @@ def forward(q, k, v, *, causal=False, softmax_scale=None, q_rope=None, k_rope=No
     cu_seqlens_q / cu_seqlens_k -> O [Tq,Hq,Dv], LSE [Hq,Tq]. Optional rope
     parts q_rope [..,Hq,R] and k_rope [..,R] (one per token, shared by heads);
     fp8 e4m3 q/k need per-token fp32 scales q_scale [B,Hq,Sq] / [Hq,Tq] and
-    k_scale [B,Hkv,Sk] / [Hkv,Tk]. Asynchronous on ``stream`` (default: the
-    current torch stream).
+    k_scale [B,Hkv,Sk] / [Hkv,Tk]. ``num_splits``: split-KV key ranges per
+    query tile (0 = the library's choice, 1 = off; unmasked fixed-length
+    problems only). Asynchronous on ``stream`` (default: the current torch
+    stream).
     """
     for name, t in (("q", q), ("k", k), ("v", v), ("q_rope", q_rope), ("k_rope", k_rope), ("q_scale", q_scale),
                     ("k_scale", k_scale), ("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
@@ -202,12 +215,15 @@ def forward(q, k, v, *, causal=False, softmax_scale=None, q_rope=None, k_rope=No
             lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=dev)
         else:
             lse = torch.empty((q.shape[0], q.shape[2], q.shape[1]), dtype=torch.float32, device=dev)
-    if workspace is None:
-        workspace = default_workspace(dev)
     p = make_params(q, k, v, causal=causal, softmax_scale=softmax_scale, q_rope=q_rope, k_rope=k_rope,
                     q_scale=q_scale, k_scale=k_scale, cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k,
                     max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k, out=out, lse=lse,
-                    workspace=workspace, backend=backend)
+                    workspace=workspace, backend=backend, num_splits=num_splits)
+    if workspace is None:
+        with torch.cuda.device(dev):
+            need = workspace_bytes(p)
+        workspace = default_workspace(dev, need)
+        p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel()
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
@@ -238,8 +254,9 @@ def plan(p: Params) -> PlanInfo:
     return info
 
 
-def schedule(p: Params, host_cu_seqlens_q=None):
-    """The persistent scheduler's order of work tiles, as (batch, head, tile)."""
+def schedule(p: Params, host_cu_seqlens_q=None, with_split=False):
+    """The persistent scheduler's order of work tiles, as (batch, head, tile)
+    or, with ``with_split``, (batch, head, tile, split-KV range)."""
     L = lib()
     cu = None
     cu_arr = None
@@ -251,4 +268,6 @@ def schedule(p: Params, host_cu_seqlens_q=None):
         raise AttnError(1, "bad schedule arguments")
     out = (WorkTile * max(n, 1))()
     L.attn_fwd_schedule(ctypes.byref(p), cu, out, n)
+    if with_split:
+        return [(w.batch, w.head, w.tile, w.split) for w in out[:n]]
     return [(w.batch, w.head, w.tile) for w in out[:n]]

@@ -39,6 +39,14 @@ attn_status validate(const attn_fwd_params* p) {
     return fail(ATTN_ERR_INVALID_ARG, "unknown backend %d", p->backend);
   if (p->fault_injection != 0 && p->fault_injection != 1)
     return fail(ATTN_ERR_INVALID_ARG, "unknown fault_injection %d", p->fault_injection);
+  if (p->num_splits < 0 || p->num_splits > af::kMaxSplits)
+    return fail(ATTN_ERR_INVALID_ARG, "num_splits %d outside [0, %d]", p->num_splits, af::kMaxSplits);
+  if (p->num_splits >= 2) {
+    if (p->backend != ATTN_BACKEND_TCGEN05)
+      return fail(ATTN_ERR_UNSUPPORTED, "split-KV runs on the tcgen05 backend only");
+    if (p->causal) return fail(ATTN_ERR_UNSUPPORTED, "split-KV is not supported with the causal mask");
+    if (p->cu_seqlens_q != nullptr) return fail(ATTN_ERR_UNSUPPORTED, "split-KV is not supported for packed sequences");
+  }
   if (p->batch < 0 || p->seqlen_q < 0 || p->seqlen_k < 0 || p->total_q < 0 || p->total_k < 0)
     return fail(ATTN_ERR_INVALID_ARG, "negative size");
   if (p->num_heads_q <= 0 || p->num_heads_kv <= 0)
@@ -72,8 +80,9 @@ attn_status validate(const attn_fwd_params* p) {
       return fail(ATTN_ERR_INVALID_ARG, "negative stride");
   }
   if (p->backend == ATTN_BACKEND_TCGEN05) {
-    if (p->workspace == nullptr || p->workspace_bytes < ATTN_FWD_WORKSPACE_BYTES)
-      return fail(ATTN_ERR_INVALID_ARG, "workspace of at least %d bytes is required", ATTN_FWD_WORKSPACE_BYTES);
+    const size_t need = attn_fwd_workspace_bytes(p);
+    if (p->workspace == nullptr || p->workspace_bytes < need)
+      return fail(ATTN_ERR_INVALID_ARG, "workspace of at least %zu bytes is required", need);
     if (reinterpret_cast<uintptr_t>(p->workspace) & 255u)
       return fail(ATTN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
     // TMA: 16-byte aligned bases and strides that are multiples of 16 bytes.
@@ -142,6 +151,29 @@ int32_t kv_chunk_for(const attn_fwd_params* p) {
 int64_t work_tiles_bound(const attn_fwd_params* p) {
   const int64_t T = af::tiles_for(p->seqlen_q, af::kRowsPerTile);
   return (int64_t)p->batch * p->num_heads_q * T;
+}
+
+// Key ranges per query tile for `p` (1 = no split-KV). Explicit counts are
+// capped at the number of key tiles; 0 asks for the scheduler's choice on
+// fixed-length unmasked problems.
+int32_t resolve_splits(const attn_fwd_params* p) {
+  if (p == nullptr || p->num_splits == 1 || p->num_splits < 0 || p->num_splits > af::kMaxSplits ||
+      p->backend != ATTN_BACKEND_TCGEN05 || p->causal || p->cu_seqlens_q != nullptr || p->batch <= 0 ||
+      p->seqlen_q <= 0 || p->seqlen_k <= 0 || p->num_heads_q <= 0)
+    return 1;
+  const int32_t kv_tiles = af::tiles_for(p->seqlen_k, af::kBlockN);
+  if (p->num_splits >= 2) return p->num_splits < kv_tiles ? p->num_splits : kv_tiles;
+  return af::choose_splits(work_tiles_bound(p), kv_tiles, sm_count_cached(), af::kMaxSplits);
+}
+
+size_t round256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+// Split-KV partial results in the workspace, after the 256 bytes of counters.
+size_t lse_part_bytes(const attn_fwd_params* p, int32_t splits) {
+  return round256((size_t)splits * p->batch * p->num_heads_q * p->seqlen_q * sizeof(float));
+}
+size_t o_part_bytes(const attn_fwd_params* p, int32_t splits) {
+  return (size_t)splits * p->batch * p->seqlen_q * p->num_heads_q * p->head_dim_v * sizeof(float);
 }
 
 // ---------------------------------------------------------------- tensor maps
@@ -240,11 +272,36 @@ attn_status launch_tc05(const attn_fwd_params* p, cudaStream_t stream) {
   prm.scale_log2 = p->softmax_scale * 1.4426950408889634f;
   prm.withhold_v = p->fault_injection == 1 ? 1 : 0;
   prm.timeout_ns = prm.withhold_v ? 200000000ull : 2000000000ull;
-  int64_t bound = work_tiles_bound(p);
+  const int32_t splits = resolve_splits(p);
+  prm.num_splits = splits;
+  prm.kv_tiles = af::tiles_for(p->seqlen_k, af::kBlockN);
+  if (splits > 1) {
+    uint8_t* ws = static_cast<uint8_t*>(p->workspace);
+    prm.lse_part = reinterpret_cast<float*>(ws + ATTN_FWD_WORKSPACE_BYTES);
+    prm.o_part = reinterpret_cast<float*>(ws + ATTN_FWD_WORKSPACE_BYTES + lse_part_bytes(p, splits));
+    prm.total_work *= splits;
+  }
+  const int64_t bound = work_tiles_bound(p) * splits;
   if (bound <= 0) return ATTN_OK;
   const int grid = (int)(bound < sm_count_cached() ? bound : sm_count_cached());
   cudaError_t e = af::tc05_launch(variant, p->causal != 0, prm, grid, stream);
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "tcgen05 kernel launch failed: %s", cudaGetErrorString(e));
+  if (splits > 1) {
+    af::SplitCombineParams cp;
+    cp.lse_part = prm.lse_part;
+    cp.o_part = prm.o_part;
+    cp.o = prm.o;
+    cp.lse = p->lse;
+    cp.splits = splits;
+    cp.batch = p->batch;
+    cp.seqlen_q = p->seqlen_q;
+    cp.heads_q = p->num_heads_q;
+    cp.o_stride_b = p->o_stride[0];
+    cp.o_stride_t = p->o_stride[1];
+    cp.o_stride_h = p->o_stride[2];
+    e = af::splitkv_combine_launch(cp, p->head_dim_v, stream);
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "split-KV merge launch failed: %s", cudaGetErrorString(e));
+  }
   return ATTN_OK;
 }
 
@@ -269,8 +326,9 @@ void attn_fwd_params_init(attn_fwd_params* p) {
 }
 
 size_t attn_fwd_workspace_bytes(const attn_fwd_params* p) {
-  (void)p;
-  return ATTN_FWD_WORKSPACE_BYTES;
+  const int32_t splits = resolve_splits(p);
+  if (splits <= 1) return ATTN_FWD_WORKSPACE_BYTES;
+  return ATTN_FWD_WORKSPACE_BYTES + lse_part_bytes(p, splits) + o_part_bytes(p, splits);
 }
 
 size_t attn_fwd_params_size(void) { return sizeof(attn_fwd_params); }
@@ -321,11 +379,13 @@ attn_status attn_fwd_plan(const attn_fwd_params* p, attn_fwd_plan_info* out) {
     out->work_tiles = (int64_t)((p->seqlen_q + 3) / 4) * p->num_heads_q * p->batch;
     out->grid = (int32_t)out->work_tiles;
     out->block = 128;
+    out->num_splits = 1;
     return ATTN_OK;
   }
   const af::Tc05Config c = af::tc05_config(tc05_variant(p));
   out->rows_per_tile = af::kRowsPerTile;
-  out->work_tiles = work_tiles_bound(p);
+  out->num_splits = resolve_splits(p);
+  out->work_tiles = work_tiles_bound(p) * out->num_splits;
   const int sms = sm_count_cached();
   out->grid = (int32_t)(out->work_tiles < sms ? out->work_tiles : sms);
   out->block = c.threads;
@@ -348,13 +408,15 @@ int64_t attn_fwd_schedule(const attn_fwd_params* p, const int32_t* host_cu_seqle
       out[n].batch = w.b;
       out[n].head = w.h;
       out[n].tile = w.t;
+      out[n].split = w.split;
     }
     ++n;
   };
   if (host_cu_seqlens_q == nullptr) {
     const int32_t T = af::tiles_for(p->seqlen_q, af::kRowsPerTile);
-    const int64_t total = (int64_t)p->batch * p->num_heads_q * T;
-    for (int64_t w = 0; w < total; ++w) emit(af::decode_fixed(w, T, p->num_heads_q, group, chunk));
+    const int32_t splits = resolve_splits(p);
+    const int64_t total = (int64_t)p->batch * p->num_heads_q * T * splits;
+    for (int64_t w = 0; w < total; ++w) emit(af::decode_fixed(w, T, splits, p->num_heads_q, group, chunk));
     return n;
   }
   for (int b = 0; b < p->batch; ++b) {

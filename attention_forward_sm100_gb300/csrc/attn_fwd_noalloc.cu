@@ -57,7 +57,12 @@ attn_status static_workspace(void** out) {
 
 extern "C" attn_status attn_fwd_noalloc(const attn_fwd_params* p, attn_stream_t stream) {
   if (p == nullptr) return af::report_error(ATTN_ERR_INVALID_ARG, "params is NULL");
-  const size_t need = attn_fwd_workspace_bytes(p);
+  attn_fwd_params q = *p;
+  // Split-KV partial results do not fit the fixed array: the automatic
+  // choice becomes "no split" here, and an explicit split count is refused
+  // below as needing more scratch.
+  if (q.num_splits == 0) q.num_splits = 1;
+  const size_t need = attn_fwd_workspace_bytes(&q);
   if (need > kStaticWorkspaceBytes)
     return af::report_error(ATTN_ERR_UNSUPPORTED,
                             "this call needs %zu bytes of scratch, more than the %zu-byte static workspace", need,
@@ -65,7 +70,6 @@ extern "C" attn_status attn_fwd_noalloc(const attn_fwd_params* p, attn_stream_t 
   void* ws = nullptr;
   attn_status st = static_workspace(&ws);
   if (st != ATTN_OK) return st;
-  attn_fwd_params q = *p;
   q.workspace = ws;
   q.workspace_bytes = kStaticWorkspaceBytes;
   attn_fwd_plan_info info;

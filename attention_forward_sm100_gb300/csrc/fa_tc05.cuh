@@ -67,6 +67,8 @@ enum BarId : int {
   BAR_FIXED = 27         // then K_FULL[NK], K_EMPTY[NK], V_FULL[NV], V_EMPTY[NV]
 };
 
+constexpr int kSlotBytes = 48;   // shared-memory bytes of one SchedSlot entry
+
 // Consumers of a scheduler slot: the two MMA lanes, 2 softmax warpgroups, the
 // correction warpgroup and the V producer lane.
 constexpr uint32_t kSchedConsumers = 2 + 128 + 128 + 128 + 1;
@@ -93,8 +95,8 @@ struct Tc05Traits {
   static constexpr int OFF_RCPL = OFF_V + NV * V_STAGE_BYTES;       // float [NQ][BM]
   static constexpr int OFF_KS = OFF_RCPL + NQ * BM * 4;             // float [NQ][2][BN] (fp8)
   static constexpr int KS_BYTES = FP8 ? NQ * 2 * BN * 4 : 0;
-  static constexpr int OFF_SCHED = OFF_KS + KS_BYTES;               // 2 slots x 32 bytes
-  static constexpr int OFF_BAR = OFF_SCHED + 64;
+  static constexpr int OFF_SCHED = OFF_KS + KS_BYTES;               // 2 slots x kSlotBytes
+  static constexpr int OFF_BAR = OFF_SCHED + 2 * kSlotBytes;
   static constexpr int NUM_BARS = BAR_FIXED + 2 * NK + 2 * NV;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
@@ -128,8 +130,10 @@ struct Tc05Traits {
                 "register split exceeds the launch allocation");
 };
 
+// One decoded work tile as published to every role. With split-KV, k_start
+// and lk already describe the tile's own key range.
 struct SchedSlot {
-  int32_t valid, b, h, t, q_start, lq, k_start, lk;
+  int32_t valid, b, h, t, q_start, lq, k_start, lk, split;
 };
 
 struct Ctx {
@@ -229,10 +233,10 @@ __device__ __forceinline__ Geo tile_geo(const SchedSlot& s) {
 }
 
 __device__ __forceinline__ SchedSlot read_slot(const Ctx& c, int slot, int off_sched) {
-  const volatile int32_t* p = reinterpret_cast<const volatile int32_t*>(c.smem + off_sched + 32 * slot);
+  const volatile int32_t* p = reinterpret_cast<const volatile int32_t*>(c.smem + off_sched + kSlotBytes * slot);
   SchedSlot s;
   s.valid = p[0]; s.b = p[1]; s.h = p[2]; s.t = p[3];
-  s.q_start = p[4]; s.lq = p[5]; s.k_start = p[6]; s.lk = p[7];
+  s.q_start = p[4]; s.lq = p[5]; s.k_start = p[6]; s.lk = p[7]; s.split = p[8];
   return s;
 }
 
@@ -246,13 +250,19 @@ struct Cursor {
 __device__ __forceinline__ SchedSlot decode_work(const Tc05Params& P, int64_t w, Cursor& cur) {
   SchedSlot s;
   s.valid = 0;
-  s.b = s.h = s.t = s.q_start = s.k_start = 0;
+  s.b = s.h = s.t = s.q_start = s.k_start = s.split = 0;
   s.lq = P.seqlen_q;
   s.lk = P.seqlen_k;
   if (!P.packed) {
     if (w < P.total_work) {
-      const WorkTile wt = decode_fixed(w, P.tiles_per_seq, P.heads_q, P.group, P.kv_chunk);
-      s.valid = 1; s.b = wt.b; s.h = wt.h; s.t = wt.t;
+      const WorkTile wt = decode_fixed(w, P.tiles_per_seq, P.num_splits, P.heads_q, P.group, P.kv_chunk);
+      s.valid = 1; s.b = wt.b; s.h = wt.h; s.t = wt.t; s.split = wt.split;
+      if (P.num_splits > 1) {
+        int32_t j0, j1;
+        split_range(wt.split, P.num_splits, P.kv_tiles, &j0, &j1);
+        s.k_start = j0 * kBlockN;
+        s.lk = min(P.seqlen_k, j1 * kBlockN) - s.k_start;
+      }
     }
     return s;
   }
@@ -306,9 +316,9 @@ __device__ void role_load_qk(const Tc05Params& P, const Ctx& c) {
     const SchedSlot s = decode_work(P, w, cur);
     if (!wait_warp(c, BAR_SCHED_EMPTY + sched.idx, sched.phase ^ 1u, kRoleLoadQK)) { aborted = true; break; }
     if (lane == 0) {
-      volatile int32_t* p = reinterpret_cast<volatile int32_t*>(c.smem + T::OFF_SCHED + 32 * sched.idx);
+      volatile int32_t* p = reinterpret_cast<volatile int32_t*>(c.smem + T::OFF_SCHED + kSlotBytes * sched.idx);
       p[0] = s.valid; p[1] = s.b; p[2] = s.h; p[3] = s.t;
-      p[4] = s.q_start; p[5] = s.lq; p[6] = s.k_start; p[7] = s.lk;
+      p[4] = s.q_start; p[5] = s.lq; p[6] = s.k_start; p[7] = s.lk; p[8] = s.split;
       ptx::mbar_arrive(c.bar(BAR_SCHED_FULL + sched.idx));
     }
     __syncwarp();
@@ -588,6 +598,11 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
     const bool row_valid = qi < s.lq;
     const int lim = CAUSAL ? min(s.lk, qi + 1) : s.lk;   // keys visible to this row
     const int first_row = g.q0 + kBlockM * i;
+    // LSE row: [B][Hq][Sq] (or [Hq][Tq] packed); a split-KV range writes its
+    // partial LSE to [split][B][Hq][Sq], i.e. batch index split * B + b of
+    // the partial array.
+    const bool split_kv = !CAUSAL && P.num_splits > 1;   // the host never splits a causal problem
+    const int lse_b = split_kv ? s.split * P.batch + s.b : s.b;
     float c_row = P.scale_log2;
     int64_t ks_base = 0;
     if (T::FP8) {
@@ -597,7 +612,8 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
         qs = P.packed ? P.q_scale[(int64_t)s.h * P.total_q + s.q_start + qi]
                       : P.q_scale[((int64_t)s.b * P.heads_q + s.h) * P.seqlen_q + qi];
       c_row *= qs;
-      ks_base = P.packed ? (int64_t)hk * P.total_k + s.k_start : ((int64_t)s.b * P.heads_kv + hk) * P.seqlen_k;
+      ks_base = P.packed ? (int64_t)hk * P.total_k + s.k_start
+                         : ((int64_t)s.b * P.heads_kv + hk) * P.seqlen_k + s.k_start;
     }
     float ks_next = 0.f;
     if (T::FP8 && n > 0) ks_next = tid < s.lk ? __ldg(P.k_scale + ks_base + tid) : 0.f;
@@ -706,11 +722,13 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
       l = l * alpha + ((s0 + s1) + (s2 + s3));
       m = m_use;
     }
-    // Row statistics: LSE (natural log) here, 1/l to the epilogue.
-    if (row_valid && P.lse != nullptr) {
+    // Row statistics: LSE (natural log) here, 1/l to the epilogue. A split-KV
+    // range writes the LSE of its own keys for the merge.
+    float* const lse_dst = (!CAUSAL && P.num_splits > 1) ? P.lse_part : P.lse;
+    if (row_valid && lse_dst != nullptr) {
       const float lse = l > 0.f ? (m + ptx::lg2(l)) * 0.69314718055994531f : -INFINITY;
-      if (P.packed) P.lse[(int64_t)s.h * P.total_q + s.q_start + qi] = lse;
-      else P.lse[((int64_t)s.b * P.heads_q + s.h) * P.seqlen_q + qi] = lse;
+      if (P.packed) lse_dst[(int64_t)s.h * P.total_q + s.q_start + qi] = lse;
+      else lse_dst[((int64_t)lse_b * P.heads_q + s.h) * P.seqlen_q + qi] = lse;
     }
     if (!wait_warp(c, BAR_STATS_FREE + i, stats_phase ^ 1u, role)) return;
     stats_phase ^= 1u;
@@ -729,6 +747,15 @@ __device__ __forceinline__ void store_row_chunk(uint16_t* dst, const uint32_t (&
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int e = 0; e < 4; ++e) d[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+}
+
+// Split-KV: one 32-column chunk of a row of normalised partial O, in fp32.
+__device__ __forceinline__ void store_row_chunk_f32(float* dst, const uint32_t (&r)[32], float scale) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+    d[e] = make_float4(__uint_as_float(r[4 * e]) * scale, __uint_as_float(r[4 * e + 1]) * scale,
+                       __uint_as_float(r[4 * e + 2]) * scale, __uint_as_float(r[4 * e + 3]) * scale);
 }
 
 template <class T, bool CAUSAL>
@@ -761,13 +788,32 @@ __device__ void role_correction(const Tc05Params& P, const Ctx& c) {
         ofinal_phase[i] ^= 1u;
         ptx::tc_fence_after();
         const uint32_t tO = c.tmem + lane_base + T::tm_o(i);
+        if (!CAUSAL && P.num_splits > 1) {
+          // Split-KV range (never causal): normalised partial O in fp32 for the merge.
+          float* prow =
+              P.o_part + ((((int64_t)s.split * P.batch + s.b) * P.seqlen_q + qi) * P.heads_q + s.h) * T::DV;
+#pragma unroll 1
+          for (int q = 0; q < T::DV / 32; ++q) {
+            uint32_t r[32];
+            ptx::tmem_ld32(tO + 32 * q, r);
+            ptx::tmem_wait_ld();
+            if (row_valid) store_row_chunk_f32(prow + 32 * q, r, rl);
+          }
+        } else {
 #pragma unroll
-        for (int q = 0; q < T::DV / 32; ++q) {
-          uint32_t r[32];
-          ptx::tmem_ld32(tO + 32 * q, r);
-          ptx::tmem_wait_ld();
-          if (row_valid) store_row_chunk<T>(orow + 32 * q, r, rl);
+          for (int q = 0; q < T::DV / 32; ++q) {
+            uint32_t r[32];
+            ptx::tmem_ld32(tO + 32 * q, r);
+            ptx::tmem_wait_ld();
+            if (row_valid) store_row_chunk<T>(orow + 32 * q, r, rl);
+          }
         }
+      } else if (row_valid && !CAUSAL && P.num_splits > 1) {
+        // A split range always holds keys; kept for completeness.
+        float4* d = reinterpret_cast<float4*>(
+            P.o_part + ((((int64_t)s.split * P.batch + s.b) * P.seqlen_q + qi) * P.heads_q + s.h) * T::DV);
+#pragma unroll 1
+        for (int e = 0; e < T::DV / 4; ++e) d[e] = make_float4(0.f, 0.f, 0.f, 0.f);
       } else if (row_valid) {
         uint4* d = reinterpret_cast<uint4*>(orow);
 #pragma unroll

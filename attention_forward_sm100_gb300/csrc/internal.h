@@ -12,6 +12,7 @@ constexpr int kRowsPerTile = 256;   // query rows per work tile of the tcgen05 k
 constexpr int kBlockM = 128;        // query rows per MMA tile (one TMEM lane per row)
 constexpr int kBlockN = 128;        // keys per K/V tile
 constexpr int64_t kL2ChunkBudget = 48ll << 20;   // K/V bytes one scheduling chunk may keep in L2
+constexpr int kMaxSplits = 64;      // split-KV ranges per query tile (the merge kernel holds 2 per lane)
 
 // Workspace words (uint32 each).
 enum WorkspaceWord : int {
@@ -53,6 +54,20 @@ struct Tc05Params {
   float scale_log2;        // softmax_scale * log2(e)
   uint64_t timeout_ns;     // limit of every device wait
   int32_t withhold_v;      // testing: block 0 skips its first V tile load
+  int32_t num_splits;      // key ranges per query tile (1: no split-KV)
+  int32_t kv_tiles;        // split-KV: ceil(seqlen_k / kBlockN)
+  float* lse_part;         // split-KV: partial LSE [splits][B][Hq][Sq]
+  float* o_part;           // split-KV: partial O (normalised, fp32) [splits][B][Sq][Hq][Dv]
+};
+
+// Arguments of the split-KV merge kernel.
+struct SplitCombineParams {
+  const float* lse_part;   // [splits][B][Hq][Sq]
+  const float* o_part;     // [splits][B][Sq][Hq][Dv]
+  uint16_t* o;             // bf16 output rows
+  float* lse;              // [B][Hq][Sq] or NULL
+  int32_t splits, batch, seqlen_q, heads_q;
+  int64_t o_stride_b, o_stride_t, o_stride_h;   // elements
 };
 
 // Kernel variants of the tcgen05 path.
@@ -80,6 +95,8 @@ attn_status report_error(attn_status st, const char* fmt, ...);
 Tc05Config tc05_config(int variant);
 // Launch of one variant (defined in the per-variant translation units).
 cudaError_t tc05_launch(int variant, bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
+// Launch of the split-KV merge kernel (head_dim_v 64 or 128).
+cudaError_t splitkv_combine_launch(const SplitCombineParams& p, int head_dim_v, cudaStream_t stream);
 // Launch of the plain CUDA-core kernel.
 cudaError_t simple_launch(const attn_fwd_params& p, cudaStream_t stream);
 

@@ -1,0 +1,106 @@
+// Merge of split-KV partial results (the LSE-combine pass that the
+// "splitk_partitions" field of the SM100AttentionSMem page's configuration
+// calls for).
+//
+// With the keys of one query tile cut into S ranges, range s leaves for each
+// (row, head) its softmax-normalised partial output O_s and the natural-log
+// sum of exponentials L_s of its own scores. The exact result over all keys
+// follows from the identity
+//     L = log sum_s exp(L_s),    O = sum_s exp(L_s - L) * O_s,
+// which this kernel evaluates with the maximum of the L_s subtracted first
+// so that no exponential overflows. One warp merges one (row, head): lane k
+// holds the weights of ranges k and k + 32, and each lane accumulates
+// Dv / 32 consecutive output columns, so every partial row is read once,
+// coalesced, and O is rounded to bf16 once.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "internal.h"
+
+namespace af {
+namespace {
+
+constexpr int kCombineWarps = 8;
+
+template <int DV>
+__global__ void __launch_bounds__(kCombineWarps * 32) splitkv_combine_kernel(const SplitCombineParams p) {
+  constexpr int C = DV / 32;   // output columns per lane
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);   // (b, i, h), h fastest
+  const int64_t rows = (int64_t)p.batch * p.seqlen_q * p.heads_q;
+  if (row >= rows) return;
+  const int h = (int)(row % p.heads_q);
+  const int64_t bi = row / p.heads_q;
+  const int i = (int)(bi % p.seqlen_q);
+  const int b = (int)(bi / p.seqlen_q);
+  // Partial LSE layout [S][B][Hq][Sq]; partial O layout [S][B][Sq][Hq][Dv].
+  const int64_t lse_row = ((int64_t)b * p.heads_q + h) * p.seqlen_q + i;
+  const int64_t lse_split = (int64_t)p.batch * p.heads_q * p.seqlen_q;
+  float l0 = -INFINITY, l1 = -INFINITY;
+  if (lane < p.splits) l0 = p.lse_part[lane * lse_split + lse_row];
+  if (lane + 32 < p.splits) l1 = p.lse_part[(lane + 32) * lse_split + lse_row];
+  float mx = fmaxf(l0, l1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + (int64_t)b * p.o_stride_b + (int64_t)i * p.o_stride_t + (int64_t)h * p.o_stride_h;
+  if (mx == -INFINITY) {   // no key reached this row in any range
+    for (int c = 0; c < C; ++c) orow[C * lane + c] = __float2bfloat16(0.f);
+    if (p.lse != nullptr && lane == 0) p.lse[lse_row] = -INFINITY;
+    return;
+  }
+  float w0 = expf(l0 - mx), w1 = expf(l1 - mx);
+  float sum = w0 + w1;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float inv = 1.f / sum;
+  w0 *= inv;
+  w1 *= inv;
+  float acc[C];
+#pragma unroll
+  for (int c = 0; c < C; ++c) acc[c] = 0.f;
+  const int64_t o_split = rows * DV;
+  const float* src = p.o_part + row * DV + C * lane;
+  for (int s = 0; s < p.splits; ++s) {
+    const float w = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
+    const float* x = src + s * o_split;
+    if (C == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(x);
+      acc[0] = fmaf(w, v.x, acc[0]);
+      acc[1] = fmaf(w, v.y, acc[1]);
+      acc[2] = fmaf(w, v.z, acc[2]);
+      acc[3] = fmaf(w, v.w, acc[3]);
+    } else {
+      const float2 v = *reinterpret_cast<const float2*>(x);
+      acc[0] = fmaf(w, v.x, acc[0]);
+      acc[1] = fmaf(w, v.y, acc[1]);
+    }
+  }
+  if (C == 4) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0], acc[1]), hi = __floats2bfloat162_rn(acc[2], acc[3]);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(orow + C * lane) = pk;
+  } else {
+    *reinterpret_cast<__nv_bfloat162*>(orow + C * lane) = __floats2bfloat162_rn(acc[0], acc[1]);
+  }
+  if (p.lse != nullptr && lane == 0) p.lse[lse_row] = mx + logf(sum);
+}
+
+}  // namespace
+
+cudaError_t splitkv_combine_launch(const SplitCombineParams& p, int head_dim_v, cudaStream_t stream) {
+  const int64_t rows = (int64_t)p.batch * p.seqlen_q * p.heads_q;
+  if (rows == 0) return cudaSuccess;
+  const int64_t blocks = (rows + kCombineWarps - 1) / kCombineWarps;
+  if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
+  if (head_dim_v == 128)
+    splitkv_combine_kernel<128><<<(unsigned)blocks, kCombineWarps * 32, 0, stream>>>(p);
+  else if (head_dim_v == 64)
+    splitkv_combine_kernel<64><<<(unsigned)blocks, kCombineWarps * 32, 0, stream>>>(p);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+}  // namespace af

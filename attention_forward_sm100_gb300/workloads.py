@@ -93,7 +93,10 @@ def draw_lengths(batch: int, lo: int, hi: int, seed: int) -> list:
     return torch.randint(lo, hi + 1, (batch,), generator=g).tolist()
 
 
-# The five workloads, named by what they are.
+# The workloads, named by what they are. The last one is a short-query,
+# long-key shape (a prefill chunk of 256 rows against a 32k-token cache, GQA
+# 32/8, no mask) whose few query tiles cannot fill the GPU: the shape that
+# split-KV exists for.
 def _workloads():
     return {
         "mha_b1_h2_s128_d64_noncausal": AttnSpec(
@@ -112,6 +115,9 @@ def _workloads():
         "fp8_b2_h32_s8192_d128_causal": AttnSpec(
             batch=2, heads_q=32, heads_kv=32, seqlen_q=8192, seqlen_k=8192,
             d_qk=128, d_v=128, causal=True, seed=4, qk_dtype="fp8"),
+        "splitkv_b1_hq32_hkv8_sq256_sk32768_d128_noncausal": AttnSpec(
+            batch=1, heads_q=32, heads_kv=8, seqlen_q=256, seqlen_k=32768,
+            d_qk=128, d_v=128, causal=False, seed=5),
     }
 
 

@@ -283,6 +283,13 @@ def main():
               cu_seqlens_k=d.get("cu_seqlens_k"), max_seqlen_q=max(lq), max_seqlen_k=max(lk), out=out, lse=lse)
     in_bytes = sum(t.numel() * t.element_size() for t in d.values() if isinstance(t, torch.Tensor))
     stream = torch.cuda.current_stream(dev)
+    # Kernels per call: the attention kernel, plus the merge kernel when the
+    # library splits the keys of each query tile (split-KV).
+    prm = pkg.make_params(d["q"], d["k"], d["v"], **kw)
+    ws = pkg.default_workspace(dev, pkg.workspace_bytes(prm))
+    prm.workspace, prm.workspace_bytes = ws.data_ptr(), ws.numel()
+    num_splits = pkg.plan(prm).num_splits
+    launches_per_step = 2 if num_splits > 1 else 1
 
     def step():
         pkg.forward(d["q"], d["k"], d["v"], stream=stream, **kw)
@@ -374,6 +381,7 @@ def main():
             "config": {"workload": args.workload, "batch": spec.batch, "heads_q": spec.heads_q,
                        "heads_kv": spec.heads_kv, "seqlen": spec.seqlen_q, "head_dim_qk": spec.d_qk + spec.rope,
                        "head_dim_v": spec.d_v, "causal": spec.causal, "flops_per_step": flops,
+                       "seqlen_k": spec.seqlen_k, "num_splits": num_splits,
                        "l2": "inputs larger than L2" if in_bytes > L2_BYTES else "inputs fit in L2 (no flush)",
                        "parallelism": f"replicas x{world}"},
             "pct_of_peak": 100.0 * value / world / peak,
@@ -382,7 +390,7 @@ def main():
                          "traffic": profiled_traffic(args.workload)},
             "kernel_ms": kernel_ms,
             "clocks": clk,
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * launches_per_step,
             "e2e": e2e,
             "cpu_baseline": cpu,
         }

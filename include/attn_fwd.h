@@ -20,7 +20,8 @@
  *   - Every pointer in attn_fwd_params is a DEVICE pointer owned by the caller.
  *     The library allocates no memory and keeps no mutable global state.
  *   - attn_fwd() validates, encodes TMA descriptors on the host and enqueues
- *     one kernel on `stream`; it returns without synchronising. Invalid
+ *     one kernel on `stream` (two with split-KV: the partial ranges, then
+ *     their merge); it returns without synchronising. Invalid
  *     arguments are reported before anything is enqueued and no memory is
  *     touched. No C++ exception crosses this boundary.
  *   - Kernel-side failures (a bounded wait that ran out) are recorded in the
@@ -57,8 +58,9 @@ typedef enum attn_backend {
   ATTN_BACKEND_SIMPLE = 1       /* plain fp32 CUDA-core kernel, for cross-checking only */
 } attn_backend;
 
-/* Bytes of workspace attn_fwd needs; the workspace holds the persistent
- * scheduler's work counter and the device error record. */
+/* Bytes of workspace attn_fwd needs without split-KV; the workspace holds the
+ * persistent scheduler's work counter and the device error record (and, with
+ * split-KV, the partial results: see attn_fwd_workspace_bytes). */
 #define ATTN_FWD_WORKSPACE_BYTES 256
 
 /* Size of the scratch array that attn_fwd_noalloc keeps inside the library
@@ -78,7 +80,7 @@ typedef struct attn_fwd_params {
   const int32_t *cu_seqlens_k; /* packed only: [B+1] prefix offsets of the key rows */
   void *o;              /* fixed [B,Sq,Hq,Dv] / packed [Tq,Hq,Dv]; bf16, written */
   float *lse;           /* [B,Hq,Sq] / [Hq,Tq] contiguous fp32, written; may be NULL */
-  void *workspace;      /* >= ATTN_FWD_WORKSPACE_BYTES device bytes, 256-byte aligned,
+  void *workspace;      /* >= attn_fwd_workspace_bytes(p) device bytes, 256-byte aligned,
                            zero-filled once before its first use; every call leaves it
                            zeroed again. Calls that share a workspace must not overlap. */
   size_t workspace_bytes;
@@ -112,6 +114,15 @@ typedef struct attn_fwd_params {
    * bounded device wait runs out (limit 200 ms instead of 2 s), the kernel
    * aborts cleanly and attn_fwd_check reports ATTN_ERR_DEVICE_TIMEOUT. */
   int32_t fault_injection;
+
+  /* Split-KV: number of key ranges each query tile is split into (the
+   * "splitk_partitions" of the SM100AttentionSMem page's configuration).
+   * 0 = chosen by the library (splits only non-causal fixed-length problems
+   * with too few query tiles to fill the GPU), 1 = off, n >= 2 = n ranges.
+   * Each range writes a normalised partial O and its LSE into the workspace
+   * (attn_fwd_workspace_bytes grows accordingly) and a second small kernel
+   * merges them. Causal problems do not split (UNSUPPORTED if n >= 2). */
+  int32_t num_splits;
 } attn_fwd_params;
 
 /* Query results of attn_fwd_plan (host only; no GPU needed). */
@@ -125,6 +136,7 @@ typedef struct attn_fwd_plan_info {
   int32_t k_stages;         /* depth of the K ring */
   int32_t v_stages;         /* depth of the V ring */
   int32_t tmem_columns;     /* tensor-memory columns allocated per CTA */
+  int32_t num_splits;       /* key ranges per query tile (1 = no split-KV) */
 } attn_fwd_plan_info;
 
 /* One work tile as the persistent scheduler hands it out. */
@@ -132,6 +144,7 @@ typedef struct attn_work_tile {
   int32_t batch;            /* sequence b */
   int32_t head;             /* query head h */
   int32_t tile;             /* query tile t: rows [t*rows_per_tile, (t+1)*rows_per_tile) */
+  int32_t split;            /* split-KV key range (0 without split-KV) */
 } attn_work_tile;
 
 /* Fills `p` with zeros and the defaults (bf16, tcgen05 backend). */
@@ -140,7 +153,12 @@ void attn_fwd_params_init(attn_fwd_params *p);
 /* sizeof(attn_fwd_params) as compiled into the library (binding check). */
 size_t attn_fwd_params_size(void);
 
-/* Workspace bytes needed for `p` (currently ATTN_FWD_WORKSPACE_BYTES). */
+/* Workspace bytes needed for `p`: ATTN_FWD_WORKSPACE_BYTES, plus with
+ * split-KV (n ranges) the partial LSE, n*B*Hq*Sq floats rounded up to 256
+ * bytes, and the partial O, n*B*Sq*Hq*Dv floats. The automatic split count
+ * (num_splits = 0) depends on the SM count of the current device: call this
+ * with the device current that attn_fwd will run on. Never fails (an invalid
+ * `p` or NULL gives ATTN_FWD_WORKSPACE_BYTES). */
 size_t attn_fwd_workspace_bytes(const attn_fwd_params *p);
 
 /* Validates `p` and enqueues the forward on `stream`. Asynchronous. Errors:
@@ -159,8 +177,9 @@ attn_status attn_fwd(const attn_fwd_params *p, attn_stream_t stream);
  * calls that overlap on the GPU (concurrent streams, or other threads) race
  * on it and must be serialised by the caller. Device-side wait timeouts of
  * this variant are not reported (there is no caller-visible error record).
- * Returns UNSUPPORTED if a call would need more scratch than the array holds,
- * otherwise as attn_fwd. */
+ * num_splits = 0 means "no split" here; an explicit split count needs more
+ * scratch than the array holds. Returns UNSUPPORTED if a call would need more
+ * scratch than the array holds, otherwise as attn_fwd. */
 attn_status attn_fwd_noalloc(const attn_fwd_params *p, attn_stream_t stream);
 
 /* Synchronises `stream`, reads and clears the device error record of

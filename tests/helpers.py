@@ -70,7 +70,7 @@ def assert_within(err, dtype):
         assert err[key] <= bound, f"{key}={err[key]:.3e} exceeds {bound:.1e} ({err})"
 
 
-def run_lib(inputs, backend="tcgen05", device="cuda"):
+def run_lib(inputs, backend="tcgen05", device="cuda", num_splits=0):
     """Runs the library on a workload input dict; returns (O, LSE) as CPU tensors."""
     import attention_forward_sm100_gb300 as pkg
     spec = inputs["spec"]
@@ -81,7 +81,7 @@ def run_lib(inputs, backend="tcgen05", device="cuda"):
                          q_rope=d.get("q_rope"), k_rope=d.get("k_rope"), q_scale=d.get("q_scale"),
                          k_scale=d.get("k_scale"), cu_seqlens_q=d.get("cu_seqlens_q"),
                          cu_seqlens_k=d.get("cu_seqlens_k"), max_seqlen_q=max(lq + [0]),
-                         max_seqlen_k=max(lk + [0]), backend=backend)
+                         max_seqlen_k=max(lk + [0]), backend=backend, num_splits=num_splits)
     pkg.check(device=dev)
     return o.cpu(), lse.cpu()
 

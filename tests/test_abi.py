@@ -166,3 +166,88 @@ def test_schedule_packed(pkg):
     # sequences in order
     bs = [b for b, _, _ in order]
     assert bs == sorted(bs)
+
+
+# ---------------------------------------------------------------- split-KV
+def _split_params(pkg, B=1, Sq=256, Sk=32768, Hq=32, Hkv=8, causal=False, splits=0, ws_bytes=1 << 30, packed=False):
+    q = _Fake((B, Sq, Hq, 128), ptr=1 << 20)
+    k = _Fake((B, Sk, Hkv, 128), ptr=2 << 20)
+    v = _Fake((B, Sk, Hkv, 128), ptr=3 << 20)
+    o = _Fake((B, Sq, Hq, 128), ptr=4 << 20)
+    ws = _Fake((ws_bytes,), dtype=torch.uint8, ptr=5 << 20)
+    kw = {}
+    if packed:
+        q = _Fake((B * Sq, Hq, 128), ptr=1 << 20)
+        k = _Fake((B * Sk, Hkv, 128), ptr=2 << 20)
+        v = _Fake((B * Sk, Hkv, 128), ptr=3 << 20)
+        o = _Fake((B * Sq, Hq, 128), ptr=4 << 20)
+        kw = dict(cu_seqlens_q=_Fake((B + 1,), ptr=6 << 20), cu_seqlens_k=_Fake((B + 1,), ptr=7 << 20),
+                  max_seqlen_q=Sq, max_seqlen_k=Sk)
+    return pkg.make_params(q, k, v, causal=causal, out=o, lse=None, workspace=ws, num_splits=splits, **kw)
+
+
+def test_split_kv_explicit_plan_and_workspace(pkg):
+    p = _split_params(pkg, B=2, Sq=300, Sk=1000, Hq=4, Hkv=2, splits=3)
+    info = pkg.plan(p)
+    assert info.num_splits == 3
+    assert info.work_tiles == 2 * 4 * 2 * 3          # B * Hq * ceil(300/256) * splits
+    lse = 3 * 2 * 4 * 300 * 4
+    lse = (lse + 255) // 256 * 256
+    assert pkg.workspace_bytes(p) == 256 + lse + 3 * 2 * 300 * 4 * 128 * 4
+
+
+def test_split_kv_count_capped_at_key_tiles(pkg):
+    p = _split_params(pkg, Sq=64, Sk=300, Hq=2, Hkv=2, splits=9)   # 3 key tiles
+    assert pkg.plan(p).num_splits == 3
+
+
+def test_split_kv_automatic_choice(pkg):
+    # A short-query / long-key problem with too few query tiles for the GPU splits ...
+    auto = pkg.plan(_split_params(pkg)).num_splits
+    assert 2 <= auto <= 64
+    # ... one with many query tiles, a causal one or a packed one does not.
+    assert pkg.plan(_split_params(pkg, B=4, Sq=4096, Sk=4096, Hq=16, Hkv=16)).num_splits == 1
+    assert pkg.plan(_split_params(pkg, causal=True)).num_splits == 1
+    assert pkg.plan(_split_params(pkg, packed=True)).num_splits == 1
+    assert pkg.workspace_bytes(_split_params(pkg, causal=True)) == 256
+    # a single key tile leaves nothing to split
+    assert pkg.plan(_split_params(pkg, Sk=100)).num_splits == 1
+
+
+@pytest.mark.parametrize("case,status", [("causal", 2), ("packed", 2), ("simple", 2), ("too_many", 1),
+                                         ("negative", 1), ("small_workspace", 1)])
+def test_split_kv_rejections(pkg, case, status):
+    if case == "causal":
+        p = _split_params(pkg, causal=True, splits=2)
+    elif case == "packed":
+        p = _split_params(pkg, packed=True, splits=2)
+    elif case == "simple":
+        p = _split_params(pkg, splits=2)
+        p.backend = 1
+    elif case == "too_many":
+        p = _split_params(pkg, splits=65)
+    elif case == "negative":
+        p = _split_params(pkg, splits=-1)
+    else:
+        p = _split_params(pkg, splits=4, ws_bytes=4096)
+    with pytest.raises(pkg.AttnError) as e:
+        pkg.plan(p)
+    assert e.value.status == status
+
+
+@pytest.mark.parametrize("B,Sq,Hq,Hkv,Sk,splits", [(1, 256, 32, 8, 32768, 0), (2, 700, 4, 2, 1000, 3),
+                                                    (1, 1, 2, 1, 5000, 64)])
+def test_schedule_with_splits_covers_each_piece_once(pkg, B, Sq, Hq, Hkv, Sk, splits):
+    p = _split_params(pkg, B=B, Sq=Sq, Sk=Sk, Hq=Hq, Hkv=Hkv, splits=splits)
+    n = pkg.plan(p).num_splits
+    assert n > 1
+    order = pkg.schedule(p, with_split=True)
+    T = (Sq + 255) // 256
+    expect = {(b, h, t, r) for b in range(B) for h in range(Hq) for t in range(T) for r in range(n)}
+    assert len(order) == len(expect) and set(order) == expect
+    # the ranges of one query tile are handed out next to each other for a
+    # KV head's query heads (they share the K/V range in L2)
+    g = Hq // Hkv
+    for i in range(0, len(order), g):
+        blk = order[i:i + g]
+        assert len({(b, h // g, t, r) for b, h, t, r in blk}) == 1
