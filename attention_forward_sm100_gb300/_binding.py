@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn_fwd
 ATTN_OK = 0
 STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "cuda error", 4: "device timeout"}
 BACKENDS = {"tcgen05": 0, "simple": 1}
+SCHEDULES = {"dynamic": 0, "static": 1, "grid": 2}
 DTYPES = {torch.bfloat16: 0, torch.float8_e4m3fn: 1}
 WORKSPACE_BYTES = 256
 
@@ -47,6 +48,7 @@ class Params(ctypes.Structure):
         ("k_rope_stride", ctypes.c_int64 * 2),
         ("fault_injection", ctypes.c_int32),
         ("num_splits", ctypes.c_int32),
+        ("schedule", ctypes.c_int32),
     ]
 
 
@@ -137,7 +139,7 @@ def _require_cuda(name, t):
 
 def make_params(q, k, v, *, causal, softmax_scale=None, q_rope=None, k_rope=None, q_scale=None, k_scale=None,
                 cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, out=None, lse=None,
-                workspace=None, backend="tcgen05", num_splits=0) -> Params:
+                workspace=None, backend="tcgen05", num_splits=0, schedule="dynamic") -> Params:
     """attn_fwd_params for torch tensors (shapes are read, nothing is allocated)."""
     packed = cu_seqlens_q is not None
     p = Params()
@@ -162,6 +164,7 @@ def make_params(q, k, v, *, causal, softmax_scale=None, q_rope=None, k_rope=None
     p.qk_dtype = DTYPES[q.dtype]
     p.backend = BACKENDS[backend]
     p.num_splits = int(num_splits)
+    p.schedule = SCHEDULES[schedule]
     p.q, p.k, p.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
     p.q_rope, p.k_rope = _ptr(q_rope), _ptr(k_rope)
     p.q_scale, p.k_scale = _ptr(q_scale), _ptr(k_scale)
@@ -189,7 +192,7 @@ def make_params(q, k, v, *, causal, softmax_scale=None, q_rope=None, k_rope=None
 
 def forward(q, k, v, *, causal=False, softmax_scale=None, q_rope=None, k_rope=None, q_scale=None, k_scale=None,
             cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, out=None, lse=None,
-            return_lse=True, workspace=None, backend="tcgen05", stream=None, num_splits=0):
+            return_lse=True, workspace=None, backend="tcgen05", stream=None, num_splits=0, schedule="dynamic"):
     """Fused attention forward on the GPU; returns (O, LSE).
 
     Fixed length: q [B,Sq,Hq,D], k [B,Sk,Hkv,D], v [B,Sk,Hkv,Dv] -> O
@@ -199,8 +202,9 @@ def forward(q, k, v, *, causal=False, softmax_scale=None, q_rope=None, k_rope=No
     fp8 e4m3 q/k need per-token fp32 scales q_scale [B,Hq,Sq] / [Hq,Tq] and
     k_scale [B,Hkv,Sk] / [Hkv,Tk]. ``num_splits``: split-KV key ranges per
     query tile (0 = the library's choice, 1 = off; unmasked fixed-length
-    problems only). Asynchronous on ``stream`` (default: the current torch
-    stream).
+    problems only). ``schedule``: "dynamic" (default), "static" or "grid",
+    how work tiles reach CTAs (results are identical). Asynchronous on
+    ``stream`` (default: the current torch stream).
     """
     for name, t in (("q", q), ("k", k), ("v", v), ("q_rope", q_rope), ("k_rope", k_rope), ("q_scale", q_scale),
                     ("k_scale", k_scale), ("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
@@ -218,7 +222,7 @@ def forward(q, k, v, *, causal=False, softmax_scale=None, q_rope=None, k_rope=No
     p = make_params(q, k, v, causal=causal, softmax_scale=softmax_scale, q_rope=q_rope, k_rope=k_rope,
                     q_scale=q_scale, k_scale=k_scale, cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k,
                     max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k, out=out, lse=lse,
-                    workspace=workspace, backend=backend, num_splits=num_splits)
+                    workspace=workspace, backend=backend, num_splits=num_splits, schedule=schedule)
     if workspace is None:
         with torch.cuda.device(dev):
             need = workspace_bytes(p)

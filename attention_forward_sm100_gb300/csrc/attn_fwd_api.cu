@@ -39,6 +39,9 @@ attn_status validate(const attn_fwd_params* p) {
     return fail(ATTN_ERR_INVALID_ARG, "unknown backend %d", p->backend);
   if (p->fault_injection != 0 && p->fault_injection != 1)
     return fail(ATTN_ERR_INVALID_ARG, "unknown fault_injection %d", p->fault_injection);
+  if (p->schedule != ATTN_SCHEDULE_DYNAMIC && p->schedule != ATTN_SCHEDULE_STATIC &&
+      p->schedule != ATTN_SCHEDULE_GRID)
+    return fail(ATTN_ERR_INVALID_ARG, "unknown schedule %d", p->schedule);
   if (p->num_splits < 0 || p->num_splits > af::kMaxSplits)
     return fail(ATTN_ERR_INVALID_ARG, "num_splits %d outside [0, %d]", p->num_splits, af::kMaxSplits);
   if (p->num_splits >= 2) {
@@ -168,6 +171,14 @@ int32_t resolve_splits(const attn_fwd_params* p) {
 
 size_t round256(size_t n) { return (n + 255) & ~(size_t)255; }
 
+// CTAs launched for `work` work tiles: one per SM for the persistent
+// schedules, one per work tile otherwise.
+int64_t grid_for(const attn_fwd_params* p, int64_t work) {
+  if (p->schedule == ATTN_SCHEDULE_GRID) return work;
+  const int sms = sm_count_cached();
+  return work < sms ? work : sms;
+}
+
 // Split-KV partial results in the workspace, after the 256 bytes of counters.
 size_t lse_part_bytes(const attn_fwd_params* p, int32_t splits) {
   return round256((size_t)splits * p->batch * p->num_heads_q * p->seqlen_q * sizeof(float));
@@ -283,7 +294,9 @@ attn_status launch_tc05(const attn_fwd_params* p, cudaStream_t stream) {
   }
   const int64_t bound = work_tiles_bound(p) * splits;
   if (bound <= 0) return ATTN_OK;
-  const int grid = (int)(bound < sm_count_cached() ? bound : sm_count_cached());
+  if (grid_for(p, bound) > 0x7fffffffll) return fail(ATTN_ERR_UNSUPPORTED, "too many work tiles for one grid");
+  const int grid = (int)grid_for(p, bound);
+  prm.schedule = p->schedule;
   cudaError_t e = af::tc05_launch(variant, p->causal != 0, prm, grid, stream);
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "tcgen05 kernel launch failed: %s", cudaGetErrorString(e));
   if (splits > 1) {
@@ -386,8 +399,9 @@ attn_status attn_fwd_plan(const attn_fwd_params* p, attn_fwd_plan_info* out) {
   out->rows_per_tile = af::kRowsPerTile;
   out->num_splits = resolve_splits(p);
   out->work_tiles = work_tiles_bound(p) * out->num_splits;
-  const int sms = sm_count_cached();
-  out->grid = (int32_t)(out->work_tiles < sms ? out->work_tiles : sms);
+  const int64_t grid = grid_for(p, out->work_tiles);
+  if (grid > 0x7fffffffll) return fail(ATTN_ERR_UNSUPPORTED, "too many work tiles for one grid");
+  out->grid = (int32_t)grid;
   out->block = c.threads;
   out->smem_bytes = c.smem_bytes;
   out->k_stages = c.k_stages;

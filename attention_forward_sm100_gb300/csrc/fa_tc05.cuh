@@ -370,10 +370,17 @@ __device__ void role_load_qk(const Tc05Params& P, const Ctx& c) {
       }
       if (aborted) break;
     }
-    // next work index (dynamic)
-    int64_t nw = 0;
-    if (lane == 0) nw = (int64_t)gridDim.x + (int64_t)atomicAdd(&c.ws[kWsTileCounter], 1u);
-    w = __shfl_sync(kFull, nw, 0);
+    // Next work index: from the shared counter (dynamic), one grid stride on
+    // (static), or none (one CTA per work tile).
+    if (P.schedule == ATTN_SCHEDULE_DYNAMIC) {
+      int64_t nw = 0;
+      if (lane == 0) nw = (int64_t)gridDim.x + (int64_t)atomicAdd(&c.ws[kWsTileCounter], 1u);
+      w = __shfl_sync(kFull, nw, 0);
+    } else if (P.schedule == ATTN_SCHEDULE_STATIC) {
+      w += gridDim.x;
+    } else {
+      w = INT64_MAX;
+    }
   }
   if (aborted && lane == 0) {
     // Let every copy this warp issued land before the CTA exits.

@@ -68,6 +68,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--schedule", default="dynamic", choices=["dynamic", "static", "grid"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -280,7 +281,8 @@ def main():
         lse = torch.empty((spec.batch, spec.heads_q, spec.seqlen_q), dtype=torch.float32, device=dev)
     kw = dict(causal=spec.causal, softmax_scale=spec.softmax_scale, q_rope=d.get("q_rope"), k_rope=d.get("k_rope"),
               q_scale=d.get("q_scale"), k_scale=d.get("k_scale"), cu_seqlens_q=d.get("cu_seqlens_q"),
-              cu_seqlens_k=d.get("cu_seqlens_k"), max_seqlen_q=max(lq), max_seqlen_k=max(lk), out=out, lse=lse)
+              cu_seqlens_k=d.get("cu_seqlens_k"), max_seqlen_q=max(lq), max_seqlen_k=max(lk), out=out, lse=lse,
+              schedule=args.schedule)
     in_bytes = sum(t.numel() * t.element_size() for t in d.values() if isinstance(t, torch.Tensor))
     stream = torch.cuda.current_stream(dev)
     # Kernels per call: the attention kernel, plus the merge kernel when the
@@ -381,7 +383,7 @@ def main():
             "config": {"workload": args.workload, "batch": spec.batch, "heads_q": spec.heads_q,
                        "heads_kv": spec.heads_kv, "seqlen": spec.seqlen_q, "head_dim_qk": spec.d_qk + spec.rope,
                        "head_dim_v": spec.d_v, "causal": spec.causal, "flops_per_step": flops,
-                       "seqlen_k": spec.seqlen_k, "num_splits": num_splits,
+                       "seqlen_k": spec.seqlen_k, "num_splits": num_splits, "schedule": args.schedule,
                        "l2": "inputs larger than L2" if in_bytes > L2_BYTES else "inputs fit in L2 (no flush)",
                        "parallelism": f"replicas x{world}"},
             "pct_of_peak": 100.0 * value / world / peak,

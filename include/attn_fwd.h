@@ -58,6 +58,18 @@ typedef enum attn_backend {
   ATTN_BACKEND_SIMPLE = 1       /* plain fp32 CUDA-core kernel, for cross-checking only */
 } attn_backend;
 
+/* Work distribution of the tcgen05 kernel (the "mha_schedule" and
+ * "may_advance" members of the MHATileScheduler page). Every mode visits
+ * the same work tiles in the same heaviest-first order (attn_fwd_schedule)
+ * and gives bit-identical results; they differ only in how tiles reach CTAs. */
+typedef enum attn_schedule {
+  ATTN_SCHEDULE_DYNAMIC = 0,    /* persistent, one CTA per SM; each CTA takes the next work index
+                                   from an atomic counter when it finishes a tile (default) */
+  ATTN_SCHEDULE_STATIC = 1,     /* persistent, one CTA per SM; CTA c takes indices c, c + grid, ... */
+  ATTN_SCHEDULE_GRID = 2        /* one CTA per work tile, no advance; the hardware launches CTAs
+                                   in index order as SMs free up */
+} attn_schedule;
+
 /* Bytes of workspace attn_fwd needs without split-KV; the workspace holds the
  * persistent scheduler's work counter and the device error record (and, with
  * split-KV, the partial results: see attn_fwd_workspace_bytes). */
@@ -123,6 +135,9 @@ typedef struct attn_fwd_params {
    * (attn_fwd_workspace_bytes grows accordingly) and a second small kernel
    * merges them. Causal problems do not split (UNSUPPORTED if n >= 2). */
   int32_t num_splits;
+
+  /* attn_schedule; ignored by the simple backend. */
+  int32_t schedule;
 } attn_fwd_params;
 
 /* Query results of attn_fwd_plan (host only; no GPU needed). */

@@ -251,3 +251,30 @@ def test_schedule_with_splits_covers_each_piece_once(pkg, B, Sq, Hq, Hkv, Sk, sp
     for i in range(0, len(order), g):
         blk = order[i:i + g]
         assert len({(b, h // g, t, r) for b, h, t, r in blk}) == 1
+
+
+# ---------------------------------------------------------------- schedule modes
+@pytest.mark.parametrize("mode", ["dynamic", "static", "grid"])
+def test_schedule_modes_plan(pkg, mode):
+    q = _Fake((2, 4096, 16, 128), ptr=1 << 20)
+    k = _Fake((2, 4096, 16, 128), ptr=2 << 20)
+    o = _Fake((2, 4096, 16, 128), ptr=4 << 20)
+    ws = _Fake((256,), dtype=torch.uint8, ptr=5 << 20)
+    p = pkg.make_params(q, k, k, causal=True, out=o, lse=None, workspace=ws, schedule=mode)
+    info = pkg.plan(p)
+    assert info.work_tiles == 2 * 16 * 16
+    if mode == "grid":
+        assert info.grid == info.work_tiles            # one CTA per work tile
+    else:
+        assert info.grid <= 160 and info.grid < info.work_tiles   # one CTA per SM
+    # the order of work indices is the same in every mode
+    base = pkg.make_params(q, k, k, causal=True, out=o, lse=None, workspace=ws)
+    assert pkg.schedule(p) == pkg.schedule(base)
+
+
+def test_schedule_mode_rejected(pkg):
+    p = _params(pkg)
+    p.schedule = 3
+    with pytest.raises(pkg.AttnError) as e:
+        pkg.plan(p)
+    assert e.value.status == 1
