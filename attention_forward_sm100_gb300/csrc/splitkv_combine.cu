@@ -11,7 +11,8 @@
 // so that no exponential overflows. One warp merges one (row, head): lane k
 // holds the weights of ranges k and k + 32, and each lane accumulates
 // Dv / 32 consecutive output columns, so every partial row is read once,
-// coalesced, and O is rounded to bf16 once.
+// coalesced (streaming loads: nothing reads it again), and O is rounded to
+// bf16 once.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -21,6 +22,7 @@ namespace af {
 namespace {
 
 constexpr int kCombineWarps = 8;
+constexpr int kBatch = 8;   // partial rows each lane loads before accumulating
 
 template <int DV>
 __global__ void __launch_bounds__(kCombineWarps * 32) splitkv_combine_kernel(const SplitCombineParams p) {
@@ -42,7 +44,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) splitkv_combine_kernel(con
   float mx = fmaxf(l0, l1);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + (int64_t)b * p.o_stride_b + (int64_t)i * p.o_stride_t + (int64_t)h * p.o_stride_h;
+  __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + (int64_t)b * p.o_stride_b +
+                        (int64_t)i * p.o_stride_t + (int64_t)h * p.o_stride_h;
   if (mx == -INFINITY) {   // no key reached this row in any range
     for (int c = 0; c < C; ++c) orow[C * lane + c] = __float2bfloat16(0.f);
     if (p.lse != nullptr && lane == 0) p.lse[lse_row] = -INFINITY;
@@ -60,22 +63,34 @@ __global__ void __launch_bounds__(kCombineWarps * 32) splitkv_combine_kernel(con
   for (int c = 0; c < C; ++c) acc[c] = 0.f;
   const int64_t o_split = rows * DV;
   const float* src = p.o_part + row * DV + C * lane;
-  for (int s = 0; s < p.splits; ++s) {
-    const float w = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
-    const float* x = src + s * o_split;
-    if (C == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(x);
-      acc[0] = fmaf(w, v.x, acc[0]);
-      acc[1] = fmaf(w, v.y, acc[1]);
-      acc[2] = fmaf(w, v.z, acc[2]);
-      acc[3] = fmaf(w, v.w, acc[3]);
-    } else {
-      const float2 v = *reinterpret_cast<const float2*>(x);
-      acc[0] = fmaf(w, v.x, acc[0]);
-      acc[1] = fmaf(w, v.y, acc[1]);
+  // Ranges in batches of kBatch: the batch's loads are all issued before any
+  // is used, so each warp keeps kBatch row reads in flight.
+  for (int s0 = 0; s0 < p.splits; s0 += kBatch) {
+    float v[kBatch][C];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (s0 + u < p.splits) {
+        const float* x = src + (int64_t)(s0 + u) * o_split;
+        if constexpr (C == 4) {
+          const float4 t = __ldcs(reinterpret_cast<const float4*>(x));
+          v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
+        } else {
+          const float2 t = __ldcs(reinterpret_cast<const float2*>(x));
+          v[u][0] = t.x; v[u][1] = t.y;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int s = s0 + u;
+      const float w = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
+      if (s < p.splits) {
+#pragma unroll
+        for (int c = 0; c < C; ++c) acc[c] = fmaf(w, v[u][c], acc[c]);
+      }
     }
   }
-  if (C == 4) {
+  if constexpr (C == 4) {
     __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0], acc[1]), hi = __floats2bfloat162_rn(acc[2], acc[3]);
     uint2 pk;
     pk.x = *reinterpret_cast<uint32_t*>(&lo);
