@@ -42,7 +42,7 @@ class Params(ctypes.Structure):
         ("num_heads_q", ctypes.c_int32), ("num_heads_kv", ctypes.c_int32),
         ("head_dim_qk", ctypes.c_int32), ("head_dim_v", ctypes.c_int32), ("rope_depth", ctypes.c_int32),
         ("causal", ctypes.c_int32), ("softmax_scale", ctypes.c_float),
-        ("qk_dtype", ctypes.c_int32), ("backend", ctypes.c_int32),
+        ("qk_dtype", ctypes.c_int32), ("v_dtype", ctypes.c_int32), ("backend", ctypes.c_int32),
         ("q_stride", ctypes.c_int64 * 3), ("k_stride", ctypes.c_int64 * 3), ("v_stride", ctypes.c_int64 * 3),
         ("o_stride", ctypes.c_int64 * 3), ("q_rope_stride", ctypes.c_int64 * 3),
         ("k_rope_stride", ctypes.c_int64 * 2),
@@ -137,6 +137,12 @@ def _require_cuda(name, t):
         raise ValueError(f"{name} must be a CUDA tensor (this library has no CPU path)")
 
 
+def head_dim_v(v) -> int:
+    """Dv of a V tensor: its last dimension, or the depth dimension of a
+    depth-major e4m3 V ([B, Hkv, Dv, Sk])."""
+    return v.shape[-2] if v.dtype == torch.float8_e4m3fn else v.shape[-1]
+
+
 def make_params(q, k, v, *, causal, softmax_scale=None, q_rope=None, k_rope=None, q_scale=None, k_scale=None,
                 cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, out=None, lse=None,
                 workspace=None, backend="tcgen05", num_splits=0, schedule="dynamic") -> Params:
@@ -155,13 +161,17 @@ def make_params(q, k, v, *, causal, softmax_scale=None, q_rope=None, k_rope=None
         _, sk, hkv, _ = k.shape
         p.seqlen_q, p.seqlen_k = sq, sk
     rope = 0 if q_rope is None else q_rope.shape[-1]
+    v_fp8 = v.dtype == torch.float8_e4m3fn   # depth-major: [B, Hkv, Dv, Sk]
     p.batch, p.num_heads_q, p.num_heads_kv = b, hq, hkv
-    p.head_dim_qk, p.head_dim_v, p.rope_depth = d, v.shape[-1], rope
+    p.head_dim_qk, p.head_dim_v, p.rope_depth = d, head_dim_v(v), rope
     p.causal = 1 if causal else 0
     p.softmax_scale = float(softmax_scale if softmax_scale is not None else (d + rope) ** -0.5)
     if q.dtype not in DTYPES:
         raise ValueError(f"unsupported q dtype {q.dtype}")
     p.qk_dtype = DTYPES[q.dtype]
+    if v.dtype not in DTYPES:
+        raise ValueError(f"unsupported v dtype {v.dtype}")
+    p.v_dtype = DTYPES[v.dtype]
     p.backend = BACKENDS[backend]
     p.num_splits = int(num_splits)
     p.schedule = SCHEDULES[schedule]
@@ -180,7 +190,11 @@ def make_params(q, k, v, *, causal, softmax_scale=None, q_rope=None, k_rope=None
 
     p.q_stride[:] = strides3(q)
     p.k_stride[:] = strides3(k)
-    p.v_stride[:] = strides3(v)
+    if v_fp8:
+        s = v.stride()
+        p.v_stride[:] = (0, s[1], s[0]) if packed else (s[0], s[2], s[1])   # batch, depth row, head
+    else:
+        p.v_stride[:] = strides3(v)
     if out is not None:
         p.o_stride[:] = strides3(out)
     if q_rope is not None:
@@ -195,7 +209,8 @@ def forward(q, k, v, *, causal=False, softmax_scale=None, q_rope=None, k_rope=No
             return_lse=True, workspace=None, backend="tcgen05", stream=None, num_splits=0, schedule="dynamic"):
     """Fused attention forward on the GPU; returns (O, LSE).
 
-    Fixed length: q [B,Sq,Hq,D], k [B,Sk,Hkv,D], v [B,Sk,Hkv,Dv] -> O
+    Fixed length: q [B,Sq,Hq,D], k [B,Sk,Hkv,D], v [B,Sk,Hkv,Dv] (e4m3 v:
+    depth-major [B,Hkv,Dv,Sk], with e4m3 q/k; P is then rounded to e4m3) -> O
     [B,Sq,Hq,Dv] bf16, LSE [B,Hq,Sq] fp32. Packed: q [Tq,Hq,D] etc. with int32
     cu_seqlens_q / cu_seqlens_k -> O [Tq,Hq,Dv], LSE [Hq,Tq]. Optional rope
     parts q_rope [..,Hq,R] and k_rope [..,R] (one per token, shared by heads);
@@ -213,7 +228,7 @@ def forward(q, k, v, *, causal=False, softmax_scale=None, q_rope=None, k_rope=No
     packed = cu_seqlens_q is not None
     dev = q.device
     if out is None:
-        out = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=torch.bfloat16, device=dev)
+        out = torch.empty(q.shape[:-1] + (head_dim_v(v),), dtype=torch.bfloat16, device=dev)
     if lse is None and return_lse:
         if packed:
             lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=dev)

@@ -35,6 +35,8 @@ attn_status validate(const attn_fwd_params* p) {
   if (p == nullptr) return fail(ATTN_ERR_INVALID_ARG, "params is NULL");
   if (p->qk_dtype != ATTN_DTYPE_BF16 && p->qk_dtype != ATTN_DTYPE_FP8_E4M3)
     return fail(ATTN_ERR_INVALID_ARG, "unknown qk_dtype %d", p->qk_dtype);
+  if (p->v_dtype != ATTN_DTYPE_BF16 && p->v_dtype != ATTN_DTYPE_FP8_E4M3)
+    return fail(ATTN_ERR_INVALID_ARG, "unknown v_dtype %d", p->v_dtype);
   if (p->backend != ATTN_BACKEND_TCGEN05 && p->backend != ATTN_BACKEND_SIMPLE)
     return fail(ATTN_ERR_INVALID_ARG, "unknown backend %d", p->backend);
   if (p->fault_injection != 0 && p->fault_injection != 1)
@@ -77,6 +79,14 @@ attn_status validate(const attn_fwd_params* p) {
       return fail(ATTN_ERR_INVALID_ARG, "fp8 Q/K need q_scale and k_scale");
     if (p->rope_depth > 0) return fail(ATTN_ERR_UNSUPPORTED, "fp8 Q/K with a rope part");
   }
+  if (p->v_dtype == ATTN_DTYPE_FP8_E4M3) {
+    if (p->qk_dtype != ATTN_DTYPE_FP8_E4M3) return fail(ATTN_ERR_UNSUPPORTED, "fp8 V needs fp8 Q/K");
+    if (packed) return fail(ATTN_ERR_UNSUPPORTED, "fp8 V supports fixed-length sequences only");
+    if (p->head_dim_qk != 128 || p->head_dim_v != 128)
+      return fail(ATTN_ERR_UNSUPPORTED, "fp8 V supports Dqk = Dv = 128 only");
+    if (p->v_stride[1] % 16)
+      return fail(ATTN_ERR_INVALID_ARG, "fp8 V: the depth-row stride must be a multiple of 16 bytes");
+  }
   for (int i = 0; i < 3; ++i) {
     if (p->q_stride[i] < 0 || p->k_stride[i] < 0 || p->v_stride[i] < 0 || p->o_stride[i] < 0 ||
         p->q_rope_stride[i] < 0)
@@ -92,8 +102,9 @@ attn_status validate(const attn_fwd_params* p) {
     const int es = qk_elem_bytes(p);
     if (!aligned16(p->q) || !aligned16(p->k) || !aligned16(p->v))
       return fail(ATTN_ERR_INVALID_ARG, "q, k, v must be 16-byte aligned");
+    const int ves = p->v_dtype == ATTN_DTYPE_FP8_E4M3 ? 1 : 2;
     for (int i = packed ? 1 : 0; i < 3; ++i) {
-      if ((p->q_stride[i] * es) % 16 || (p->k_stride[i] * es) % 16 || (p->v_stride[i] * 2) % 16)
+      if ((p->q_stride[i] * es) % 16 || (p->k_stride[i] * es) % 16 || (p->v_stride[i] * ves) % 16)
         return fail(ATTN_ERR_INVALID_ARG, "q/k/v strides must be multiples of 16 bytes");
     }
     if (p->rope_depth > 0) {
@@ -123,7 +134,8 @@ attn_status validate(const attn_fwd_params* p) {
 }
 
 int tc05_variant(const attn_fwd_params* p) {
-  if (p->qk_dtype == ATTN_DTYPE_FP8_E4M3) return af::kVarFp8D128;
+  if (p->qk_dtype == ATTN_DTYPE_FP8_E4M3)
+    return p->v_dtype == ATTN_DTYPE_FP8_E4M3 ? af::kVarFp8QkvD128 : af::kVarFp8D128;
   if (p->head_dim_qk == 64) return af::kVarD64;
   return p->rope_depth ? af::kVarD128Rope64 : af::kVarD128;
 }
@@ -147,7 +159,8 @@ int sm_count_cached() {
 }
 
 int32_t kv_chunk_for(const attn_fwd_params* p) {
-  const int64_t row = (int64_t)(p->head_dim_qk * qk_elem_bytes(p)) + 2ll * p->rope_depth + 2ll * p->head_dim_v;
+  const int64_t row = (int64_t)(p->head_dim_qk * qk_elem_bytes(p)) + 2ll * p->rope_depth +
+                      (p->v_dtype == ATTN_DTYPE_FP8_E4M3 ? 1ll : 2ll) * p->head_dim_v;
   return af::choose_kv_chunk(p->seqlen_k, row, p->num_heads_kv, af::kL2ChunkBudget);
 }
 
@@ -229,6 +242,28 @@ attn_status make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt,
   return ATTN_OK;
 }
 
+// Depth-major fp8 V, [B][Hkv][Dv][Sk] with the keys contiguous: 4-D map over
+// (key, depth, head, batch); box {128 keys, Dv rows, 1, 1}, 128-byte swizzle,
+// so one box is the K-major B operand of the P.V product.
+attn_status make_map_vt(CUtensorMap* map, const attn_fwd_params* p) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
+  const int64_t sk = p->seqlen_k > 0 ? p->seqlen_k : 1;
+  const int64_t sd = p->v_stride[1];
+  const int64_t sh = p->num_heads_kv > 1 ? p->v_stride[2] : sd * p->head_dim_v;
+  const int64_t sb = p->batch > 1 ? p->v_stride[0] : sh * p->num_heads_kv;
+  cuuint64_t dims[4] = {(cuuint64_t)sk, (cuuint64_t)p->head_dim_v, (cuuint64_t)p->num_heads_kv,
+                        (cuuint64_t)p->batch};
+  cuuint64_t strides[3] = {(cuuint64_t)sd, (cuuint64_t)sh, (cuuint64_t)sb};
+  cuuint32_t box[4] = {(cuuint32_t)af::kBlockN, (cuuint32_t)p->head_dim_v, 1u, 1u};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(p->v), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (%d) for fp8 V", (int)r);
+  return ATTN_OK;
+}
+
 attn_status launch_tc05(const attn_fwd_params* p, cudaStream_t stream) {
   const bool packed = p->cu_seqlens_q != nullptr;
   const int variant = tc05_variant(p);
@@ -247,9 +282,12 @@ attn_status launch_tc05(const attn_fwd_params* p, cudaStream_t stream) {
   if ((st = make_map(&prm.tm_k, p->k, qk_t, es, p->head_dim_qk, p->num_heads_kv, tk, nb, p->k_stride[2],
                      p->k_stride[1], p->k_stride[0], box_qk)) != ATTN_OK)
     return st;
-  if ((st = make_map(&prm.tm_v, p->v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->head_dim_v, p->num_heads_kv, tk, nb,
-                     p->v_stride[2], p->v_stride[1], p->v_stride[0], 64)) != ATTN_OK)
+  if (p->v_dtype == ATTN_DTYPE_FP8_E4M3) {
+    if ((st = make_map_vt(&prm.tm_v, p)) != ATTN_OK) return st;
+  } else if ((st = make_map(&prm.tm_v, p->v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->head_dim_v, p->num_heads_kv,
+                            tk, nb, p->v_stride[2], p->v_stride[1], p->v_stride[0], 64)) != ATTN_OK) {
     return st;
+  }
   if (p->rope_depth > 0) {
     if ((st = make_map(&prm.tm_qr, p->q_rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->rope_depth, p->num_heads_q,
                        tq, nb, p->q_rope_stride[2], p->q_rope_stride[1], p->q_rope_stride[0], 64)) != ATTN_OK)

@@ -73,21 +73,25 @@ constexpr int kSlotBytes = 48;   // shared-memory bytes of one SchedSlot entry
 // correction warpgroup and the V producer lane.
 constexpr uint32_t kSchedConsumers = 2 + 128 + 128 + 128 + 1;
 
-template <int DQK_, int DR_, int DV_, bool FP8_>
+template <int DQK_, int DR_, int DV_, bool FP8_, bool V8_ = false>
 struct Tc05Traits {
   static constexpr int DQK = DQK_, DR = DR_, DV = DV_;
   static constexpr bool FP8 = FP8_;
+  // e4m3 V, depth-major in global memory: a V stage is Dv rows of 128 keys
+  // (K-major B operand of P.V) and P is rounded to e4m3 for kind::f8f6f4.
+  static constexpr bool V8 = V8_;
+  static_assert(!V8 || (FP8 && DV == 128), "e4m3 V needs e4m3 Q/K and Dv = 128");
   static constexpr int BM = kBlockM, BN = kBlockN, NQ = 2;
   static constexpr int QK_CHUNK_ELEMS = FP8 ? 128 : 64;   // elements of one 128-byte swizzle row
   static constexpr int QK_CHUNKS = DQK / QK_CHUNK_ELEMS;
   static constexpr int R_CHUNKS = DR / 64;
-  static constexpr int V_CHUNKS = DV / 64;
+  static constexpr int V_CHUNKS = V8 ? 1 : DV / 64;   // TMA boxes per V stage
   static constexpr int CHUNK_BYTES = 128 * 128;           // 128 rows x 128 bytes
   static constexpr int Q_TILE_BYTES = (QK_CHUNKS + R_CHUNKS) * CHUNK_BYTES;
   static constexpr int K_STAGE_BYTES = (QK_CHUNKS + R_CHUNKS) * CHUNK_BYTES;
-  static constexpr int V_STAGE_BYTES = V_CHUNKS * CHUNK_BYTES;
+  static constexpr int V_STAGE_BYTES = V8 ? DV * 128 : V_CHUNKS * CHUNK_BYTES;
   static constexpr int NK = DR > 0 ? 2 : (FP8 ? 4 : (DQK == 64 ? 4 : 3));
-  static constexpr int NV = DR > 0 ? 1 : (FP8 ? 3 : (DQK == 64 ? 4 : 2));
+  static constexpr int NV = DR > 0 ? 1 : (V8 ? 4 : (FP8 ? 3 : (DQK == 64 ? 4 : 2)));
 
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = NQ * Q_TILE_BYTES;
@@ -117,7 +121,12 @@ struct Tc05Traits {
 
   static constexpr uint32_t IDESC_S =
       FP8 ? ptx::idesc_f32acc(0, 0, false, false, 128, 128) : ptx::idesc_f32acc(1, 1, false, false, 128, 128);
-  static constexpr uint32_t IDESC_PV = ptx::idesc_f32acc(1, 1, false, true, 128, DV);
+  static constexpr uint32_t IDESC_PV =
+      V8 ? ptx::idesc_f32acc(0, 0, false, false, 128, DV) : ptx::idesc_f32acc(1, 1, false, true, 128, DV);
+  // P.V instructions per half tile of 64 keys (K = 16 per bf16 instruction, 32 per e4m3).
+  static constexpr int PV_INSTR_HALF = V8 ? 2 : 4;
+  // TMEM columns of one half of P (64 keys as bf16 pairs or e4m3 quads).
+  static constexpr int P_COLS_HALF = V8 ? 16 : 32;
   // MMA instructions of one S = Q K^T (K = 16 per bf16 instruction, 32 per fp8).
   static constexpr int S_INSTR = FP8 ? DQK / 32 : (DQK + DR) / 16;
   // S instructions issued after handing the turn to the other issuer: enough
@@ -425,9 +434,15 @@ __device__ void role_load_v(const Tc05Params& P, const Ctx& c) {
         const uint32_t dst = c.sbase + T::OFF_V + vr.idx * T::V_STAGE_BYTES;
         const int row = s.k_start + kBlockN * j;
         ptx::mbar_expect_tx(bar, T::V_STAGE_BYTES);
+        if (T::V8) {
+          // depth-major e4m3 V: coordinates (key, depth row, head, batch); the
+          // key coordinate is a multiple of 128 (fixed-length sequences only)
+          ptx::tma_load_4d(dst, &P.tm_v, bar, row, 0, hk, vb);
+        } else {
 #pragma unroll
-        for (int ch = 0; ch < T::V_CHUNKS; ++ch)
-          ptx::tma_load_4d(dst + ch * T::CHUNK_BYTES, &P.tm_v, bar, ch * 64, hk, row, vb);
+          for (int ch = 0; ch < T::V_CHUNKS; ++ch)
+            ptx::tma_load_4d(dst + ch * T::CHUNK_BYTES, &P.tm_v, bar, ch * 64, hk, row, vb);
+        }
       }
       v_fill_parity[vr.idx] = vr.phase;
       v_used[vr.idx] = v_used[vr.idx] || !withhold;
@@ -471,11 +486,21 @@ template <class T, int HALF>
 __device__ __forceinline__ void issue_pv(const Ctx& c, int i, uint32_t vstage, bool accumulate) {
   constexpr uint32_t HI = ptx::sdesc_hi_sw128(1024);
   const uint32_t d = c.tmem + T::tm_o(i);
-  const uint32_t a = c.tmem + T::tm_s(i);
-  const uint32_t va = ptx::sdesc_lo(ptx::opaque(c.sbase + T::OFF_V + vstage * T::V_STAGE_BYTES), T::CHUNK_BYTES);
+  const uint32_t a = c.tmem + T::tm_s(i);   // P: 8 TMEM columns per instruction (16 bf16 / 32 e4m3 keys)
+  if (T::V8) {
+    // K-major V stage (Dv rows x 128 keys): 32 keys = 32 bytes per instruction
+    const uint32_t va = ptx::sdesc_lo(ptx::opaque(c.sbase + T::OFF_V + vstage * T::V_STAGE_BYTES), 16);
 #pragma unroll
-  for (int kk = 4 * HALF; kk < 4 * HALF + 4; ++kk)
-    ptx::mma_bf16_ts_lo<HI, T::IDESC_PV>(d, a + kk * 8, va + kk * (2048 >> 4), (accumulate || kk > 0) ? 1u : 0u);
+    for (int kk = 2 * HALF; kk < 2 * HALF + 2; ++kk)
+      ptx::mma_fp8_ts_lo<HI, T::IDESC_PV>(d, a + kk * 8, va + kk * 2, (accumulate || kk > 0) ? 1u : 0u);
+  } else {
+    // MN-major V stage (128 keys x Dv): 16 keys = 2048 bytes per instruction
+    const uint32_t va =
+        ptx::sdesc_lo(ptx::opaque(c.sbase + T::OFF_V + vstage * T::V_STAGE_BYTES), T::CHUNK_BYTES);
+#pragma unroll
+    for (int kk = 4 * HALF; kk < 4 * HALF + 4; ++kk)
+      ptx::mma_bf16_ts_lo<HI, T::IDESC_PV>(d, a + kk * 8, va + kk * (2048 >> 4), (accumulate || kk > 0) ? 1u : 0u);
+  }
 }
 
 // One MMA-issuing warp per Q tile (warp 12 for tile 0, warp 13 for tile 1).
@@ -691,8 +716,10 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
       uint64_t acc0 = 0, acc1 = 0;   // (+0.0f, +0.0f) pairs
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        // P for keys [64*half, 64*half + 64) -> 32 packed bf16 pairs.
-        uint32_t pk[32];
+        // P for keys [64*half, 64*half + 64) -> 32 packed bf16 pairs (or 16
+        // e4m3 quads).
+        uint32_t pk[T::P_COLS_HALF];
+        [[maybe_unused]] float q0 = 0.f, q1 = 0.f;   // e4m3: the previous pair of the quad
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int el = 64 * half + 2 * e;
@@ -701,9 +728,16 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
           const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
           if (e & 1) acc1 = ptx::f2_add(acc1, ptx::f2_pack(p0, p1));
           else acc0 = ptx::f2_add(acc0, ptx::f2_pack(p0, p1));
-          pk[e] = ptx::pack_bf16(p0, p1);
+          if constexpr (T::V8) {
+            if (e & 1) pk[e >> 1] = ptx::pack_e4m3x4(q0, q1, p0, p1);
+            q0 = p0;
+            q1 = p1;
+          } else {
+            pk[e] = ptx::pack_bf16(p0, p1);
+          }
         }
-        ptx::tmem_st32(tS + 32 * half, pk);
+        if constexpr (T::V8) ptx::tmem_st16(tS + T::P_COLS_HALF * half, pk);
+        else ptx::tmem_st32(tS + T::P_COLS_HALF * half, pk);
         if (half == 0 && __any_sync(kFull, alpha != 1.f)) {
           // Correction: the running max moved (rare with the 2^8 headroom), so
           // rescale this warp's rows of O_i before the next P V accumulates
@@ -964,10 +998,12 @@ using TraitsD64 = Tc05Traits<64, 0, 64, false>;
 using TraitsD128 = Tc05Traits<128, 0, 128, false>;
 using TraitsD128R64 = Tc05Traits<128, 64, 128, false>;
 using TraitsFp8D128 = Tc05Traits<128, 0, 128, true>;
+using TraitsFp8QkvD128 = Tc05Traits<128, 0, 128, true, true>;
 
 cudaError_t tc05_launch_d64(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
 cudaError_t tc05_launch_d128(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
 cudaError_t tc05_launch_d128r64(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
 cudaError_t tc05_launch_fp8d128(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
+cudaError_t tc05_launch_fp8qkvd128(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
 
 }  // namespace af

@@ -77,7 +77,8 @@ enum Tc05Variant : int {
   kVarD128 = 1,       // bf16, Dqk = Dv = 128
   kVarD128Rope64 = 2, // bf16, Dqk = 128 + rope 64, Dv = 128
   kVarFp8D128 = 3,    // fp8 e4m3 Q/K, Dqk = Dv = 128
-  kVarCount = 4
+  kVarFp8QkvD128 = 4, // fp8 e4m3 Q/K/V (depth-major V, P rounded to e4m3), Dqk = Dv = 128
+  kVarCount = 5
 };
 
 struct Tc05Config {

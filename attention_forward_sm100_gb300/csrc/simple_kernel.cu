@@ -1,6 +1,6 @@
 // Plain fp32 CUDA-core attention forward, used only to cross-check the
 // tcgen05 kernel and the host-side argument handling (strides, packed
-// sequences, GQA, rope, FP8 scales, LSE layout). One warp owns one query row;
+// sequences, GQA, rope, FP8 scales, depth-major FP8 V, LSE layout). One warp owns one query row;
 // each lane scores one key of a 32-key chunk, the chunk's softmax update is a
 // warp reduction, and each lane accumulates Dv/32 output columns.
 #include <cuda_bf16.h>
@@ -42,6 +42,7 @@ __global__ void __launch_bounds__(kWarps * 32) simple_attn_kernel(const attn_fwd
   const int hk = h / (p.num_heads_q / p.num_heads_kv);
   const int dq = p.head_dim_qk, dr = p.rope_depth, dv = p.head_dim_v;
   const int fp8 = p.qk_dtype == ATTN_DTYPE_FP8_E4M3;
+  const bool v_fp8 = p.v_dtype == ATTN_DTYPE_FP8_E4M3;   // weights stay fp32 here (no P rounding)
   const int64_t bq = packed ? 0 : b, tq = q_base_tok + i;
 
   // Q row (nope then rope) into shared memory, as fp32.
@@ -97,12 +98,23 @@ __global__ void __launch_bounds__(kWarps * 32) simple_attn_kernel(const attn_fwd
     for (int jj = 0; jj < nj; ++jj) {
       const float w = __shfl_sync(0xffffffffu, pj, jj);
       const int64_t tk = k_base_tok + j0 + jj;
-      const int64_t vb = (packed ? 0 : (int64_t)b) * p.v_stride[0] + tk * p.v_stride[1] + (int64_t)hk * p.v_stride[2];
-      const __nv_bfloat16* vv = static_cast<const __nv_bfloat16*>(p.v);
+      if (v_fp8) {
+        // depth-major e4m3 V: [B, Hkv, Dv, Sk], keys contiguous
+        const int64_t vb = (int64_t)b * p.v_stride[0] + (int64_t)hk * p.v_stride[2] + tk;
 #pragma unroll
-      for (int c = 0; c < kMaxD / 32; ++c) {
-        const int d = c * 32 + lane;
-        if (d < dv) acc[c] = fmaf(w, __bfloat162float(vv[vb + d]), acc[c]);
+        for (int c = 0; c < kMaxD / 32; ++c) {
+          const int d = c * 32 + lane;
+          if (d < dv) acc[c] = fmaf(w, load_qk(p.v, vb + (int64_t)d * p.v_stride[1], 1), acc[c]);
+        }
+      } else {
+        const int64_t vb =
+            (packed ? 0 : (int64_t)b) * p.v_stride[0] + tk * p.v_stride[1] + (int64_t)hk * p.v_stride[2];
+        const __nv_bfloat16* vv = static_cast<const __nv_bfloat16*>(p.v);
+#pragma unroll
+        for (int c = 0; c < kMaxD / 32; ++c) {
+          const int d = c * 32 + lane;
+          if (d < dv) acc[c] = fmaf(w, __bfloat162float(vv[vb + d]), acc[c]);
+        }
       }
     }
     m = m_new;

@@ -8,6 +8,7 @@ Tc05Config tc05_config(int variant) {
     case kVarD64: return tc05_config_t<TraitsD64>();
     case kVarD128: return tc05_config_t<TraitsD128>();
     case kVarD128Rope64: return tc05_config_t<TraitsD128R64>();
+    case kVarFp8QkvD128: return tc05_config_t<TraitsFp8QkvD128>();
     default: return tc05_config_t<TraitsFp8D128>();
   }
 }
@@ -18,6 +19,7 @@ cudaError_t tc05_launch(int variant, bool causal, const Tc05Params& prm, int gri
     case kVarD128: return tc05_launch_d128(causal, prm, grid, stream);
     case kVarD128Rope64: return tc05_launch_d128r64(causal, prm, grid, stream);
     case kVarFp8D128: return tc05_launch_fp8d128(causal, prm, grid, stream);
+    case kVarFp8QkvD128: return tc05_launch_fp8qkvd128(causal, prm, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -1,0 +1,8 @@
+// Instantiation of the tcgen05 attention kernel for one head-dimension variant.
+#include "fa_tc05.cuh"
+
+namespace af {
+cudaError_t tc05_launch_fp8qkvd128(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream) {
+  return tc05_launch_t<TraitsFp8QkvD128>(causal, prm, grid, stream);
+}
+}  // namespace af

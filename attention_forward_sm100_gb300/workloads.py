@@ -12,7 +12,10 @@ Recipe (the reading taken for every workload):
     k_nope, k_rope, v), cast to bf16 with round-to-nearest-even;
   * FP8 workloads draw Q and K in fp32 and quantise each (token, head) vector
     to float8_e4m3fn with an fp32 scale = amax / 448 (amax = 0 -> scale 1);
-    the quantised value is clamp(x / scale, -448, 448) rounded to e4m3.
+    the quantised value is clamp(x / scale, -448, 448) rounded to e4m3;
+  * all-FP8 workloads also round V (drawn after K, N(0,1)) to e4m3 without a
+    scale (clamp to +-448, nearest even) and store it depth-major, each row
+    of keys padded with zeros to a multiple of 16.
 
 Layouts: Q/K/V/O are [B, S, H, D] (fixed length) or [T, H, D] (packed, with
 int32 cu_seqlens of length B + 1). The shared K rope part is [B, S, R] or
@@ -44,6 +47,7 @@ class AttnSpec:
     seed: int
     rope: int = 0            # rope depth R (K rope shared by all heads)
     qk_dtype: str = "bf16"   # "bf16" or "fp8"
+    v_dtype: str = "bf16"    # "bf16", or "fp8": e4m3 V stored depth-major [B, Hkv, Dv, Sk]
     lengths_q: Optional[Sequence[int]] = None   # packed layout when set
     lengths_k: Optional[Sequence[int]] = None   # defaults to lengths_q
     scale: Optional[float] = None               # defaults to 1/sqrt(d_qk + rope)
@@ -93,10 +97,11 @@ def draw_lengths(batch: int, lo: int, hi: int, seed: int) -> list:
     return torch.randint(lo, hi + 1, (batch,), generator=g).tolist()
 
 
-# The workloads, named by what they are. The last one is a short-query,
-# long-key shape (a prefill chunk of 256 rows against a 32k-token cache, GQA
-# 32/8, no mask) whose few query tiles cannot fill the GPU: the shape that
-# split-KV exists for.
+# The workloads, named by what they are. The last two are additions: the
+# FP8 workload with V rounded to e4m3 as well (same seed, so Q, K and V hold
+# the same draws), and a short-query, long-key shape (a prefill chunk of 256
+# rows against a 32k-token cache, GQA 32/8, no mask) whose few query tiles
+# cannot fill the GPU: the shape that split-KV exists for.
 def _workloads():
     return {
         "mha_b1_h2_s128_d64_noncausal": AttnSpec(
@@ -115,6 +120,9 @@ def _workloads():
         "fp8_b2_h32_s8192_d128_causal": AttnSpec(
             batch=2, heads_q=32, heads_kv=32, seqlen_q=8192, seqlen_k=8192,
             d_qk=128, d_v=128, causal=True, seed=4, qk_dtype="fp8"),
+        "fp8qkv_b2_h32_s8192_d128_causal": AttnSpec(
+            batch=2, heads_q=32, heads_kv=32, seqlen_q=8192, seqlen_k=8192,
+            d_qk=128, d_v=128, causal=True, seed=4, qk_dtype="fp8", v_dtype="fp8"),
         "splitkv_b1_hq32_hkv8_sq256_sk32768_d128_noncausal": AttnSpec(
             batch=1, heads_q=32, heads_kv=8, seqlen_q=256, seqlen_k=32768,
             d_qk=128, d_v=128, causal=False, seed=5),
@@ -143,6 +151,27 @@ def _scales_token_contiguous(scale: torch.Tensor, varlen: bool) -> torch.Tensor:
     if varlen:
         return scale.transpose(0, 1).contiguous()
     return scale.permute(0, 2, 1).contiguous()
+
+
+def v_token_major(v: torch.Tensor) -> torch.Tensor:
+    """V as [B, Sk, Hkv, Dv] (a view): depth-major e4m3 V is permuted back."""
+    if v.dtype == torch.float8_e4m3fn:
+        return v.permute(0, 3, 1, 2)
+    return v
+
+
+def to_device(inputs: dict, device) -> dict:
+    """Copies every tensor of an input dict to ``device`` keeping its strides
+    (a padded view such as the depth-major e4m3 V stays padded)."""
+    out = {}
+    for name, t in inputs.items():
+        if isinstance(t, torch.Tensor):
+            d = torch.empty_strided(t.size(), t.stride(), dtype=t.dtype, device=device)
+            d.copy_(t)
+            out[name] = d
+        else:
+            out[name] = t
+    return out
 
 
 def make_inputs(spec: AttnSpec) -> dict:
@@ -186,7 +215,20 @@ def make_inputs(spec: AttnSpec) -> dict:
             raise ValueError("fp8 with a rope part is not a defined workload")
         q32 = randn(*qshape, spec.d_qk)
         k32 = randn(*kshape, spec.d_qk)
-        v = randn(*kshape, spec.d_v).to(torch.bfloat16)
+        v32 = randn(*kshape, spec.d_v)
+        if spec.v_dtype == "fp8":
+            if spec.varlen:
+                raise ValueError("e4m3 V is defined for fixed-length workloads only")
+            v8 = torch.clamp(v32, -FP8_E4M3_MAX, FP8_E4M3_MAX).to(torch.float8_e4m3fn)
+            # [B, Sk, Hkv, Dv] -> [B, Hkv, Dv, Sk]; the rows of keys are padded
+            # to a multiple of 16 bytes (the alignment a TMA row stride needs)
+            # and v is the [..., :Sk] view.
+            sk_pad = (spec.seqlen_k + 15) // 16 * 16
+            vt = torch.zeros((spec.batch, spec.heads_kv, spec.d_v, sk_pad), dtype=torch.float8_e4m3fn)
+            vt[..., :spec.seqlen_k] = v8.permute(0, 2, 3, 1)
+            v = vt[..., :spec.seqlen_k]
+        else:
+            v = v32.to(torch.bfloat16)
         q8, qs = quantize_fp8_per_token(q32)
         k8, ks = quantize_fp8_per_token(k32)
         out.update(q=q8, k=k8, v=v,

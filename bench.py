@@ -85,9 +85,12 @@ def load_peaks():
 
 
 def peak_tflops(spec, peaks):
-    """Dense tensor peak for the workload's MMA mix (bf16 burst; FP8 QK^T
-    counted at 2x the bf16 rate, i.e. half the FLOPs at 2x, blended)."""
+    """Dense tensor peak for the workload's MMA mix (bf16 burst; FP8 runs at
+    2x the bf16 rate: all-FP8 at 2x, FP8 QK^T with bf16 P.V blended as half
+    the FLOPs at 2x)."""
     bf16 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    if spec.v_dtype == "fp8":
+        return 2.0 * bf16
     if spec.qk_dtype == "fp8":
         return 2.0 / (1.0 / (2.0 * bf16) + 1.0 / bf16)
     return bf16
@@ -156,7 +159,8 @@ def cpu_baseline(spec, inputs, seconds):
 
     cores = len(os.sched_getaffinity(0))
     lq, lk = spec.seq_lengths()
-    q, k, v = f64(inputs["q"]), f64(inputs["k"]), f64(inputs["v"])
+    from attention_forward_sm100_gb300.workloads import v_token_major
+    q, k, v = f64(inputs["q"]), f64(inputs["k"]), f64(v_token_major(inputs["v"]))
     qr, kr = f64(inputs.get("q_rope")), f64(inputs.get("k_rope"))
     qs, ks = f64(inputs.get("q_scale")), f64(inputs.get("k_scale"))
     cu_q = inputs.get("cu_seqlens_q")
@@ -272,7 +276,7 @@ def main():
     torch.cuda.set_device(dev)
     pkg.lib()
     inputs = W.make_inputs(spec)
-    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inputs.items()}
+    d = W.to_device(inputs, dev)
     lq, lk = spec.seq_lengths()
     out = torch.empty(d["q"].shape[:-1] + (spec.d_v,), dtype=torch.bfloat16, device=dev)
     if spec.varlen:
@@ -378,7 +382,8 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "fp8+bf16" if spec.qk_dtype == "fp8" else "bf16",
+            "vs_baseline": None,
+            "dtype": "fp8" if spec.v_dtype == "fp8" else ("fp8+bf16" if spec.qk_dtype == "fp8" else "bf16"),
             "data": "synthetic",
             "config": {"workload": args.workload, "batch": spec.batch, "heads_q": spec.heads_q,
                        "heads_kv": spec.heads_kv, "seqlen": spec.seqlen_q, "head_dim_qk": spec.d_qk + spec.rope,
@@ -388,7 +393,8 @@ def main():
                        "parallelism": f"replicas x{world}"},
             "pct_of_peak": 100.0 * value / world / peak,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "peak_source": f"bf16 burst, {peak_src}",
+                         "frac": achieved / peak,
+                         "peak_source": f"bf16 burst{' x2 (fp8)' if spec.v_dtype == 'fp8' else ''}, {peak_src}",
                          "traffic": profiled_traffic(args.workload)},
             "kernel_ms": kernel_ms,
             "clocks": clk,

@@ -14,6 +14,10 @@
  *     s_ij  = scale * q_scale_i * k_scale_j * (Q8_i . K8_j)         fp8 e4m3 Q/K
  *     LSE_i = ln sum_{j in J_i} exp(s_ij)                           natural log
  *     O_i   = sum_{j in J_i} exp(s_ij - LSE_i) * v_j                bf16, rounded once
+ *   With fp8 e4m3 V (v_dtype; Q/K fp8 too: the page's single qkv_dtype) the
+ *   weights exp(s_ij - m) are rounded to e4m3 before the P.V product (O_i is
+ *   then exact up to that rounding, at most 2^-4 relative per weight, plus
+ *   2^-10 absolute per weight relative to the row maximum); LSE_i is not.
  *   Rows with an empty J_i get O_i = 0 and LSE_i = -inf.
  *
  * Conventions
@@ -83,7 +87,9 @@ typedef struct attn_fwd_params {
   /* ---- tensors (device pointers, caller-owned) ------------------------- */
   const void *q;        /* fixed [B,Sq,Hq,Dqk] / packed [Tq,Hq,Dqk]; bf16 or fp8 (qk_dtype) */
   const void *k;        /* fixed [B,Sk,Hkv,Dqk] / packed [Tk,Hkv,Dqk]; same type as q */
-  const void *v;        /* fixed [B,Sk,Hkv,Dv] / packed [Tk,Hkv,Dv]; bf16 */
+  const void *v;        /* bf16 (v_dtype BF16): fixed [B,Sk,Hkv,Dv] / packed [Tk,Hkv,Dv];
+                           fp8 e4m3 (v_dtype FP8_E4M3, fixed length only): depth-major
+                           [B,Hkv,Dv,Sk] with the keys contiguous (v_stride: see below) */
   const void *q_rope;   /* rope_depth > 0 only: [B,Sq,Hq,R] / [Tq,Hq,R]; bf16 */
   const void *k_rope;   /* rope_depth > 0 only: [B,Sk,R] / [Tk,R]; bf16, shared by all heads */
   const float *q_scale; /* fp8 only: [B,Hq,Sq] / [Hq,Tq], contiguous fp32 */
@@ -111,10 +117,14 @@ typedef struct attn_fwd_params {
   int32_t causal;       /* non-zero: query i sees keys 0..i of its sequence */
   float softmax_scale;  /* scale of the scores; > 0 */
   int32_t qk_dtype;     /* attn_dtype */
+  int32_t v_dtype;      /* attn_dtype of v: BF16, or FP8_E4M3 (needs fp8 q/k, Dqk = Dv = 128,
+                           no rope, fixed length; no scale: V's e4m3 values are used as is) */
   int32_t backend;      /* attn_backend */
 
   /* ---- element strides: [0] batch (unused when packed), [1] token, [2] head.
-   *      The innermost dimension is contiguous. --------------------------- */
+   *      The innermost dimension is contiguous. For depth-major fp8 v,
+   *      v_stride is [0] batch, [1] depth row, [2] head (keys contiguous;
+   *      the depth-row stride must be a multiple of 16 bytes). ------------- */
   int64_t q_stride[3];
   int64_t k_stride[3];
   int64_t v_stride[3];

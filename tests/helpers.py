@@ -24,14 +24,20 @@ def oracle_args(inputs):
     )
 
 
+def v_for_oracle(inputs):
+    """V in the oracle's [B, Sk, Hkv, Dv] layout, exact float64."""
+    from attention_forward_sm100_gb300.workloads import v_token_major
+    return f64(v_token_major(inputs["v"]))
+
+
 def run_oracle(inputs):
     import oracle
-    return oracle.attention(f64(inputs["q"]), f64(inputs["k"]), f64(inputs["v"]), **oracle_args(inputs))
+    return oracle.attention(f64(inputs["q"]), f64(inputs["k"]), v_for_oracle(inputs), **oracle_args(inputs))
 
 
 def run_oracle_rows(inputs, rows):
     import oracle
-    return oracle.attention_rows(f64(inputs["q"]), f64(inputs["k"]), f64(inputs["v"]), rows,
+    return oracle.attention_rows(f64(inputs["q"]), f64(inputs["k"]), v_for_oracle(inputs), rows,
                                  **oracle_args(inputs))
 
 
@@ -75,7 +81,8 @@ def run_lib(inputs, backend="tcgen05", device="cuda", num_splits=0):
     import attention_forward_sm100_gb300 as pkg
     spec = inputs["spec"]
     dev = torch.device(device)
-    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inputs.items()}
+    from attention_forward_sm100_gb300.workloads import to_device
+    d = to_device(inputs, dev)
     lq, lk = spec.seq_lengths()
     o, lse = pkg.forward(d["q"], d["k"], d["v"], causal=spec.causal, softmax_scale=spec.softmax_scale,
                          q_rope=d.get("q_rope"), k_rope=d.get("k_rope"), q_scale=d.get("q_scale"),

@@ -278,3 +278,45 @@ def test_schedule_mode_rejected(pkg):
     with pytest.raises(pkg.AttnError) as e:
         pkg.plan(p)
     assert e.value.status == 1
+
+
+
+# ---------------------------------------------------------------- all-FP8
+@pytest.mark.parametrize("case,status", [("bf16_qk", 2), ("packed", 2), ("dv64", 2), ("row_stride", 1)])
+def test_fp8_v_rejections(pkg, case, status):
+    f8 = torch.float8_e4m3fn
+    qdt = torch.bfloat16 if case == "bf16_qk" else f8
+    dv = 64 if case == "dv64" else 128
+    sk = 333 if case == "row_stride" else 512
+    q = _Fake((1, 256, 4, 128), dtype=qdt, ptr=1 << 20)
+    k = _Fake((1, sk, 4, 128), dtype=qdt, ptr=2 << 20)
+    v = _Fake((1, 4, dv, sk), dtype=f8, ptr=3 << 20)
+    o = _Fake((1, 256, 4, dv), ptr=4 << 20)
+    sc = _Fake((1, 4, 256), dtype=torch.float32, ptr=6 << 20)
+    ws = _Fake((256,), dtype=torch.uint8, ptr=5 << 20)
+    kw = {}
+    if case == "packed":
+        q = _Fake((256, 4, 128), dtype=f8, ptr=1 << 20)
+        k = _Fake((sk, 4, 128), dtype=f8, ptr=2 << 20)
+        v = _Fake((4, dv, sk), dtype=f8, ptr=3 << 20)
+        o = _Fake((256, 4, dv), ptr=4 << 20)
+        kw = dict(cu_seqlens_q=_Fake((2,), ptr=7 << 20), cu_seqlens_k=_Fake((2,), ptr=8 << 20))
+    p = pkg.make_params(q, k, v, causal=True, out=o, lse=None, workspace=ws, q_scale=sc, k_scale=sc, **kw)
+    assert p.v_dtype == 1 and p.head_dim_v == dv
+    with pytest.raises(pkg.AttnError) as e:
+        pkg.plan(p)
+    assert e.value.status == status
+
+
+def test_fp8_v_plan(pkg):
+    f8 = torch.float8_e4m3fn
+    q = _Fake((2, 8192, 32, 128), dtype=f8, ptr=1 << 20)
+    v = _Fake((2, 32, 128, 8192), dtype=f8, ptr=3 << 20)
+    o = _Fake((2, 8192, 32, 128), ptr=4 << 20)
+    sc = _Fake((2, 32, 8192), dtype=torch.float32, ptr=6 << 20)
+    ws = _Fake((256,), dtype=torch.uint8, ptr=5 << 20)
+    p = pkg.make_params(q, q, v, causal=True, out=o, lse=None, workspace=ws, q_scale=sc, k_scale=sc)
+    assert tuple(p.v_stride) == (32 * 128 * 8192, 8192, 128 * 8192)   # batch, depth row, head
+    info = pkg.plan(p)
+    assert info.v_stages == 4 and info.k_stages == 4
+    assert info.smem_bytes <= 232448
