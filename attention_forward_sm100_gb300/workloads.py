@@ -90,6 +90,33 @@ class AttnSpec:
         """Algorithmic FLOPs: 2 * (d_qk + rope + d_v) per visible pair per head."""
         return 2 * (self.d_qk + self.rope + self.d_v) * self.visible_pairs() * self.heads_q
 
+    def flops_tile_granular(self, block_m: int = 128, block_n: int = 128) -> int:
+        """FLOPs of every block_m x block_n (query, key) tile that holds at
+        least one visible pair, counted whole (context for the exact count)."""
+        lq, lk = self.seq_lengths()
+        tiles = 0
+        for a, b in zip(lq, lk):
+            for t in range((a + block_m - 1) // block_m):
+                last_row = min(a, (t + 1) * block_m) - 1
+                keys = min(b, last_row + 1) if self.causal else b
+                tiles += (keys + block_n - 1) // block_n
+        return 2 * (self.d_qk + self.rope + self.d_v) * block_m * block_n * tiles * self.heads_q
+
+    def hbm_bytes(self) -> int:
+        """Algorithmic HBM bytes: Q, K, V (and rope parts, per-token scales)
+        read once, O (bf16) and LSE (fp32) written once."""
+        lq, lk = self.seq_lengths()
+        tq, tk = sum(lq), sum(lk)
+        qk_es = 1 if self.qk_dtype == "fp8" else 2
+        v_es = 1 if self.v_dtype == "fp8" else 2
+        n = tq * self.heads_q * (self.d_qk * qk_es + self.rope * 2)          # Q (+ q rope)
+        n += tk * self.heads_kv * self.d_qk * qk_es + tk * self.rope * 2      # K (+ shared k rope)
+        n += tk * self.heads_kv * self.d_v * v_es                             # V
+        if self.qk_dtype == "fp8":
+            n += 4 * (tq * self.heads_q + tk * self.heads_kv)                 # scales
+        n += tq * self.heads_q * (2 * self.d_v + 4)                           # O, LSE
+        return n
+
 
 def draw_lengths(batch: int, lo: int, hi: int, seed: int) -> list:
     """Sequence lengths drawn uniformly from the inclusive range [lo, hi]."""

@@ -190,9 +190,32 @@ def cpu_baseline(spec, inputs, seconds):
             break
     dt = time.perf_counter() - t0
     del np
+    full = heads == spec.batch * spec.heads_q
     return {"value": done_flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "cpu_model": cpu_model(),
             "sample": f"{heads} whole (sequence, head) problems of {spec.batch * spec.heads_q}, "
-                      f"fp64 numpy, {dt:.1f} s"}
+                      f"fp64 numpy, {dt:.1f} s",
+            "full_oracle_s": dt if full else dt * spec.flops() / done_flops,
+            "full_oracle_s_kind": "measured" if full else "extrapolated (time per FLOP x all FLOPs)"}
+
+
+def cpu_model():
+    """Model name of the host CPU (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
 
 
 def dist_setup(args):
@@ -327,6 +350,7 @@ def main():
     clk = clocks.stop()
     pkg.check(device=dev)
     per_launch = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    median_ms = statistics.median(per_launch)
     total_ms = ev[0].elapsed_time(ev[-1])
     total_ms = max_over_ranks(total_ms, world, dev)
     ms = total_ms / args.steps
@@ -389,6 +413,8 @@ def main():
                        "heads_kv": spec.heads_kv, "seqlen": spec.seqlen_q, "head_dim_qk": spec.d_qk + spec.rope,
                        "head_dim_v": spec.d_v, "causal": spec.causal, "flops_per_step": flops,
                        "seqlen_k": spec.seqlen_k, "num_splits": num_splits, "schedule": args.schedule,
+                       "flops_tile_granular": spec.flops_tile_granular(),
+                       "hbm_bytes_algorithmic": spec.hbm_bytes(),
                        "l2": "inputs larger than L2" if in_bytes > L2_BYTES else "inputs fit in L2 (no flush)",
                        "parallelism": f"replicas x{world}"},
             "pct_of_peak": 100.0 * value / world / peak,
@@ -397,11 +423,22 @@ def main():
                          "peak_source": f"bf16 burst{' x2 (fp8)' if spec.v_dtype == 'fp8' else ''}, {peak_src}",
                          "traffic": profiled_traffic(args.workload)},
             "kernel_ms": kernel_ms,
+            "median_ms": median_ms,
             "clocks": clk,
             "gpu_launches": args.steps * launches_per_step,
             "e2e": e2e,
             "cpu_baseline": cpu,
         }
+        if spec.qk_dtype == "fp8":
+            # against the nominal dense peaks as well (FP8 4.5 PF, BF16 2.25 PF)
+            line["pct_of_nominal"] = {"fp8_4500": 100.0 * value / world / 4500.0,
+                                      "bf16_2250": 100.0 * value / world / 2250.0}
+        if flops < 1e10:
+            # a problem this small is bound by launch latency, not by the tensor cores
+            hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+            line["latency"] = {"us_per_call": median_ms * 1e3,
+                               "algorithmic_gbs": spec.hbm_bytes() / (median_ms * 1e-3) / 1e9,
+                               "hbm_peak_gbs": hbm}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

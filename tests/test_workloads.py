@@ -102,3 +102,28 @@ def test_sample_rows_in_range():
     assert len(rows) == 260
     for b, h, i in rows:
         assert 0 <= b < spec.batch and 0 <= h < spec.heads_q and 0 <= i < lq[b]
+
+
+def test_hbm_bytes_table():
+    # Q, K, V (+ rope, scales) read once, O and LSE written once
+    expect = {
+        "mha_b1_h2_s128_d64_noncausal": 132_096,
+        "mha_b4_h16_s4096_d128_causal": 269_484_032,
+        "varlen_gqa_b8_hq32_hkv8_d128_causal": 569_893_632,
+        "mla_b2_h128_s4096_d128r64_causal": 1_213_202_432,
+        "fp8_b2_h32_s8192_d128_causal": 408_944_640,
+        # same with V in e4m3: one byte less per V element
+        "fp8qkv_b2_h32_s8192_d128_causal": 408_944_640 - 2 * 8192 * 32 * 128,
+    }
+    for name, n in expect.items():
+        assert W.WORKLOADS[name].hbm_bytes() == n
+
+
+def test_tile_granular_flops():
+    spec = W.WORKLOADS["mha_b4_h16_s4096_d128_causal"]
+    # 32 query tiles of 128 rows; tile t touches t + 1 key tiles
+    tiles = sum(t + 1 for t in range(32))
+    assert spec.flops_tile_granular() == 2 * 256 * 128 * 128 * tiles * 16 * 4
+    assert 1.03 < spec.flops_tile_granular() / spec.flops() < 1.032
+    nc = W.WORKLOADS["mha_b1_h2_s128_d64_noncausal"]
+    assert nc.flops_tile_granular() == nc.flops()
