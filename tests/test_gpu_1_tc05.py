@@ -100,3 +100,27 @@ def test_back_to_back_full_size_calls(name):
     for o, l in outs:
         assert torch.equal(o.view(torch.int16), o0.view(torch.int16))
         assert torch.equal(l, l0)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("qk_dtype,causal", [("bf16", True), ("bf16", False), ("fp8", True), ("fp8", False)])
+def test_growing_scores_move_the_running_max(qk_dtype, causal):
+    """Scores that grow along the key sequence (K rows scaled up with the key
+    index, or the k-scales for FP8) make the row maximum jump by far more
+    than the 2^8 headroom in most tiles, in either half of a tile: every
+    rescale path of the softmax runs."""
+    spec = S(2, 4, 2, 1100, 1100, 128, 128, causal, seed=51, qk_dtype=qk_dtype)
+    inp = W.make_inputs(spec)
+    # scale 1 + j/32: the scores' spread grows by ~4 natural units per 64 keys,
+    # so the row maximum keeps passing the 2^8 headroom (5.5 natural units)
+    grow = 1.0 + torch.arange(1100, dtype=torch.float32) / 32.0
+    if qk_dtype == "fp8":
+        inp["k_scale"] = (inp["k_scale"] * grow).contiguous()
+    else:
+        inp["k"] = (inp["k"].float() * grow[None, :, None, None]).to(torch.bfloat16)
+    # The weights concentrate on single keys, so |O| reaches max |v|; halving V
+    # (exact in bf16) keeps the bf16 roundings of P and O well inside 2e-2.
+    inp["v"] = inp["v"] * 0.5
+    err = compare_full(inp)
+    print(qk_dtype, causal, err)
+    assert_within(err, qk_dtype)
