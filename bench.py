@@ -361,6 +361,28 @@ def main():
     peaks, peak_src = load_peaks()
     peak = peak_tflops(spec, peaks)
 
+    # A problem this small is bound by the host's launch path: also time the
+    # same call captured once in a CUDA graph and replayed (100 calls per replay).
+    graph_us = None
+    if spec.flops() < 1e10:
+        g = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream(dev)
+        cs.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cs):
+            for _ in range(100):
+                pkg.forward(d["q"], d["k"], d["v"], stream=cs, **kw)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(cs):          # replay() launches on the current stream
+            g.replay()
+            torch.cuda.synchronize(dev)
+            g0.record(cs)
+            for _ in range(5):
+                g.replay()
+            g1.record(cs)
+        torch.cuda.synchronize(dev)
+        graph_us = g0.elapsed_time(g1) * 1e3 / 500
+        pkg.check(device=dev)
+
     e2e = None
     if not args.no_e2e:
         hq = inputs["q"].pin_memory()
@@ -438,7 +460,7 @@ def main():
             hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
             line["latency"] = {"us_per_call": median_ms * 1e3,
                                "algorithmic_gbs": spec.hbm_bytes() / (median_ms * 1e-3) / 1e9,
-                               "hbm_peak_gbs": hbm}
+                               "hbm_peak_gbs": hbm, "graph_replay_us_per_call": graph_us}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
