@@ -50,7 +50,6 @@ attn_status validate(const attn_fwd_params* p) {
     if (p->backend != ATTN_BACKEND_TCGEN05)
       return fail(ATTN_ERR_UNSUPPORTED, "split-KV runs on the tcgen05 backend only");
     if (p->causal) return fail(ATTN_ERR_UNSUPPORTED, "split-KV is not supported with the causal mask");
-    if (p->cu_seqlens_q != nullptr) return fail(ATTN_ERR_UNSUPPORTED, "split-KV is not supported for packed sequences");
   }
   if (p->batch < 0 || p->seqlen_q < 0 || p->seqlen_k < 0 || p->total_q < 0 || p->total_k < 0)
     return fail(ATTN_ERR_INVALID_ARG, "negative size");
@@ -170,12 +169,13 @@ int64_t work_tiles_bound(const attn_fwd_params* p) {
 }
 
 // Key ranges per query tile for `p` (1 = no split-KV). Explicit counts are
-// capped at the number of key tiles; 0 asks for the scheduler's choice on
-// fixed-length unmasked problems.
+// capped at the number of key tiles (of the longest sequence when packed);
+// 0 asks for the scheduler's choice on unmasked problems (for packed
+// sequences from the upper bound of the query tiles, B * ceil(max_len / 256)).
 int32_t resolve_splits(const attn_fwd_params* p) {
   if (p == nullptr || p->num_splits == 1 || p->num_splits < 0 || p->num_splits > af::kMaxSplits ||
-      p->backend != ATTN_BACKEND_TCGEN05 || p->causal || p->cu_seqlens_q != nullptr || p->batch <= 0 ||
-      p->seqlen_q <= 0 || p->seqlen_k <= 0 || p->num_heads_q <= 0)
+      p->backend != ATTN_BACKEND_TCGEN05 || p->causal || p->batch <= 0 || p->seqlen_q <= 0 ||
+      p->seqlen_k <= 0 || p->num_heads_q <= 0 || (p->cu_seqlens_q != nullptr && p->total_q <= 0))
     return 1;
   const int32_t kv_tiles = af::tiles_for(p->seqlen_k, af::kBlockN);
   if (p->num_splits >= 2) return p->num_splits < kv_tiles ? p->num_splits : kv_tiles;
@@ -192,12 +192,16 @@ int64_t grid_for(const attn_fwd_params* p, int64_t work) {
   return work < sms ? work : sms;
 }
 
-// Split-KV partial results in the workspace, after the 256 bytes of counters.
+// Split-KV partial results in the workspace, after the 256 bytes of counters:
+// per range one copy of the LSE layout and one fp32 O row per query row.
+size_t partial_query_rows(const attn_fwd_params* p) {
+  return p->cu_seqlens_q != nullptr ? (size_t)p->total_q : (size_t)p->batch * p->seqlen_q;
+}
 size_t lse_part_bytes(const attn_fwd_params* p, int32_t splits) {
-  return round256((size_t)splits * p->batch * p->num_heads_q * p->seqlen_q * sizeof(float));
+  return round256((size_t)splits * partial_query_rows(p) * p->num_heads_q * sizeof(float));
 }
 size_t o_part_bytes(const attn_fwd_params* p, int32_t splits) {
-  return (size_t)splits * p->batch * p->seqlen_q * p->num_heads_q * p->head_dim_v * sizeof(float);
+  return (size_t)splits * partial_query_rows(p) * p->num_heads_q * p->head_dim_v * sizeof(float);
 }
 
 // ---------------------------------------------------------------- tensor maps
@@ -347,7 +351,9 @@ attn_status launch_tc05(const attn_fwd_params* p, cudaStream_t stream) {
     cp.batch = p->batch;
     cp.seqlen_q = p->seqlen_q;
     cp.heads_q = p->num_heads_q;
-    cp.o_stride_b = p->o_stride[0];
+    cp.packed = packed ? 1 : 0;
+    cp.total_q = packed ? p->total_q : 0;
+    cp.o_stride_b = packed ? 0 : p->o_stride[0];
     cp.o_stride_t = p->o_stride[1];
     cp.o_stride_h = p->o_stride[2];
     e = af::splitkv_combine_launch(cp, p->head_dim_v, stream);
@@ -471,11 +477,16 @@ int64_t attn_fwd_schedule(const attn_fwd_params* p, const int32_t* host_cu_seqle
     for (int64_t w = 0; w < total; ++w) emit(af::decode_fixed(w, T, splits, p->num_heads_q, group, chunk));
     return n;
   }
+  const int32_t splits = resolve_splits(p);
   for (int b = 0; b < p->batch; ++b) {
     const int32_t len = host_cu_seqlens_q[b + 1] - host_cu_seqlens_q[b];
     const int32_t T = af::tiles_for(len, af::kRowsPerTile);
-    for (int64_t wl = 0; wl < (int64_t)T * p->num_heads_q; ++wl)
-      emit(af::decode_in_sequence(wl, b, T, group, p->num_heads_kv, chunk));
+    for (int64_t wl = 0; wl < (int64_t)T * splits * p->num_heads_q; ++wl) {
+      af::WorkTile w = af::decode_in_sequence(wl, b, T * splits, group, p->num_heads_kv, chunk);
+      w.split = w.t % splits;
+      w.t /= splits;
+      emit(w);
+    }
   }
   return n;
 }

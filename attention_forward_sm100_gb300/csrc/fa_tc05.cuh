@@ -282,7 +282,7 @@ __device__ __forceinline__ SchedSlot decode_work(const Tc05Params& P, int64_t w,
   while (true) {
     const int bb = cur.b + lane;
     int64_t u = 0;
-    if (bb < P.batch) u = (int64_t)tiles_for(P.cu_q[bb + 1] - P.cu_q[bb], kRowsPerTile) * P.heads_q;
+    if (bb < P.batch) u = (int64_t)tiles_for(P.cu_q[bb + 1] - P.cu_q[bb], kRowsPerTile) * P.heads_q * P.num_splits;
     int64_t incl = u;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -296,10 +296,20 @@ __device__ __forceinline__ SchedSlot decode_work(const Tc05Params& P, int64_t w,
       cur.b += L;
       const int b = cur.b;
       const int qs = P.cu_q[b], qe = P.cu_q[b + 1], ks = P.cu_k[b], ke = P.cu_k[b + 1];
-      const WorkTile wt =
-          decode_in_sequence(w - cur.base, b, tiles_for(qe - qs, kRowsPerTile), P.group, P.heads_kv, P.kv_chunk);
+      const WorkTile wt = decode_in_sequence(w - cur.base, b, tiles_for(qe - qs, kRowsPerTile) * P.num_splits,
+                                             P.group, P.heads_kv, P.kv_chunk);
       s.valid = 1; s.b = b; s.h = wt.h; s.t = wt.t;
       s.q_start = qs; s.lq = qe - qs; s.k_start = ks; s.lk = ke - ks;
+      if (P.num_splits > 1) {
+        // this sequence's own key tiles, cut like the fixed-length case (a
+        // range can be empty when the sequence has fewer key tiles than ranges)
+        s.split = wt.t % P.num_splits;
+        s.t = wt.t / P.num_splits;
+        int32_t j0, j1;
+        split_range(s.split, P.num_splits, tiles_for(ke - ks, kBlockN), &j0, &j1);
+        s.k_start = ks + j0 * kBlockN;
+        s.lk = min(ke - ks, j1 * kBlockN) - j0 * kBlockN;
+      }
       return s;
     }
     if (cur.b + 32 >= P.batch) return s;
@@ -633,11 +643,13 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
     const bool row_valid = qi < s.lq;
     const int lim = CAUSAL ? min(s.lk, qi + 1) : s.lk;   // keys visible to this row
     const int first_row = g.q0 + kBlockM * i;
-    // LSE row: [B][Hq][Sq] (or [Hq][Tq] packed); a split-KV range writes its
-    // partial LSE to [split][B][Hq][Sq], i.e. batch index split * B + b of
-    // the partial array.
+    // LSE element: [B][Hq][Sq] (or [Hq][Tq] packed); a split-KV range writes
+    // its partial LSE to copy `split` of that layout, [split][B][Hq][Sq] (or
+    // [split][Hq][Tq]).
     const bool split_kv = !CAUSAL && P.num_splits > 1;   // the host never splits a causal problem
-    const int lse_b = split_kv ? s.split * P.batch + s.b : s.b;
+    const int sp = split_kv ? s.split : 0;
+    const int64_t lse_idx = P.packed ? ((int64_t)sp * P.heads_q + s.h) * P.total_q + s.q_start + qi
+                                     : (((int64_t)sp * P.batch + s.b) * P.heads_q + s.h) * P.seqlen_q + qi;
     float c_row = P.scale_log2;
     int64_t ks_base = 0;
     if (T::FP8) {
@@ -771,8 +783,7 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
     float* const lse_dst = (!CAUSAL && P.num_splits > 1) ? P.lse_part : P.lse;
     if (row_valid && lse_dst != nullptr) {
       const float lse = l > 0.f ? (m + ptx::lg2(l)) * 0.69314718055994531f : -INFINITY;
-      if (P.packed) lse_dst[(int64_t)s.h * P.total_q + s.q_start + qi] = lse;
-      else lse_dst[((int64_t)lse_b * P.heads_q + s.h) * P.seqlen_q + qi] = lse;
+      lse_dst[lse_idx] = lse;
     }
     if (!wait_warp(c, BAR_STATS_FREE + i, stats_phase ^ 1u, role)) return;
     stats_phase ^= 1u;
@@ -791,6 +802,14 @@ __device__ __forceinline__ void store_row_chunk(uint16_t* dst, const uint32_t (&
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int e = 0; e < 4; ++e) d[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+}
+
+// Split-KV: row of the partial O array [split][rows][Hq] (rows = B*Sq, or Tq
+// when packed) of query row qi of work tile s.
+__device__ __forceinline__ int64_t partial_row(const Tc05Params& P, const SchedSlot& s, int qi) {
+  const int64_t rows = P.packed ? (int64_t)P.total_q : (int64_t)P.batch * P.seqlen_q;
+  const int64_t row = P.packed ? (int64_t)s.q_start + qi : (int64_t)s.b * P.seqlen_q + qi;
+  return ((int64_t)s.split * rows + row) * P.heads_q + s.h;
 }
 
 // Split-KV: one 32-column chunk of a row of normalised partial O, in fp32.
@@ -834,8 +853,7 @@ __device__ void role_correction(const Tc05Params& P, const Ctx& c) {
         const uint32_t tO = c.tmem + lane_base + T::tm_o(i);
         if (!CAUSAL && P.num_splits > 1) {
           // Split-KV range (never causal): normalised partial O in fp32 for the merge.
-          float* prow =
-              P.o_part + ((((int64_t)s.split * P.batch + s.b) * P.seqlen_q + qi) * P.heads_q + s.h) * T::DV;
+          float* prow = P.o_part + partial_row(P, s, qi) * T::DV;
 #pragma unroll 1
           for (int q = 0; q < T::DV / 32; ++q) {
             uint32_t r[32];
@@ -853,9 +871,9 @@ __device__ void role_correction(const Tc05Params& P, const Ctx& c) {
           }
         }
       } else if (row_valid && !CAUSAL && P.num_splits > 1) {
-        // A split range always holds keys; kept for completeness.
-        float4* d = reinterpret_cast<float4*>(
-            P.o_part + ((((int64_t)s.split * P.batch + s.b) * P.seqlen_q + qi) * P.heads_q + s.h) * T::DV);
+        // An empty key range (a short packed sequence): a zero partial row
+        // (its LSE is -inf, so the merge gives it no weight).
+        float4* d = reinterpret_cast<float4*>(P.o_part + partial_row(P, s, qi) * T::DV);
 #pragma unroll 1
         for (int e = 0; e < T::DV / 4; ++e) d[e] = make_float4(0.f, 0.f, 0.f, 0.f);
       } else if (row_valid) {

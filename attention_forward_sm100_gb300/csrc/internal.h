@@ -57,17 +57,18 @@ struct Tc05Params {
   int32_t schedule;        // attn_schedule: how the producer advances to its next work index
   int32_t num_splits;      // key ranges per query tile (1: no split-KV)
   int32_t kv_tiles;        // split-KV: ceil(seqlen_k / kBlockN)
-  float* lse_part;         // split-KV: partial LSE [splits][B][Hq][Sq]
-  float* o_part;           // split-KV: partial O (normalised, fp32) [splits][B][Sq][Hq][Dv]
+  float* lse_part;         // split-KV: partial LSE [splits][B][Hq][Sq] / [splits][Hq][Tq]
+  float* o_part;           // split-KV: partial O (normalised, fp32) [splits][rows][Hq][Dv]
 };
 
 // Arguments of the split-KV merge kernel.
 struct SplitCombineParams {
-  const float* lse_part;   // [splits][B][Hq][Sq]
-  const float* o_part;     // [splits][B][Sq][Hq][Dv]
+  const float* lse_part;   // [splits][B][Hq][Sq], packed [splits][Hq][Tq]
+  const float* o_part;     // [splits][rows][Hq][Dv], rows = B*Sq or Tq
   uint16_t* o;             // bf16 output rows
-  float* lse;              // [B][Hq][Sq] or NULL
+  float* lse;              // [B][Hq][Sq] / [Hq][Tq], or NULL
   int32_t splits, batch, seqlen_q, heads_q;
+  int32_t packed, total_q;
   int64_t o_stride_b, o_stride_t, o_stride_h;   // elements
 };
 

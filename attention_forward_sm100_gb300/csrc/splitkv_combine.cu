@@ -28,24 +28,33 @@ template <int DV>
 __global__ void __launch_bounds__(kCombineWarps * 32) splitkv_combine_kernel(const SplitCombineParams p) {
   constexpr int C = DV / 32;   // output columns per lane
   const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);   // (b, i, h), h fastest
-  const int64_t rows = (int64_t)p.batch * p.seqlen_q * p.heads_q;
+  // (query row, head) pairs, head fastest; query rows are (b, i) or packed t
+  const int64_t row = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+  const int64_t qrows = p.packed ? (int64_t)p.total_q : (int64_t)p.batch * p.seqlen_q;
+  const int64_t rows = qrows * p.heads_q;
   if (row >= rows) return;
   const int h = (int)(row % p.heads_q);
-  const int64_t bi = row / p.heads_q;
-  const int i = (int)(bi % p.seqlen_q);
-  const int b = (int)(bi / p.seqlen_q);
-  // Partial LSE layout [S][B][Hq][Sq]; partial O layout [S][B][Sq][Hq][Dv].
-  const int64_t lse_row = ((int64_t)b * p.heads_q + h) * p.seqlen_q + i;
-  const int64_t lse_split = (int64_t)p.batch * p.heads_q * p.seqlen_q;
+  const int64_t t = row / p.heads_q;
+  // Partial LSE: S copies of the LSE layout ([B][Hq][Sq] or [Hq][Tq]);
+  // partial O: [S][rows][Hq][Dv].
+  int64_t lse_row, o_off;
+  if (p.packed) {
+    lse_row = (int64_t)h * p.total_q + t;
+    o_off = t * p.o_stride_t + (int64_t)h * p.o_stride_h;
+  } else {
+    const int i = (int)(t % p.seqlen_q);
+    const int b = (int)(t / p.seqlen_q);
+    lse_row = ((int64_t)b * p.heads_q + h) * p.seqlen_q + i;
+    o_off = (int64_t)b * p.o_stride_b + (int64_t)i * p.o_stride_t + (int64_t)h * p.o_stride_h;
+  }
+  const int64_t lse_split = qrows * p.heads_q;
   float l0 = -INFINITY, l1 = -INFINITY;
   if (lane < p.splits) l0 = p.lse_part[lane * lse_split + lse_row];
   if (lane + 32 < p.splits) l1 = p.lse_part[(lane + 32) * lse_split + lse_row];
   float mx = fmaxf(l0, l1);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + (int64_t)b * p.o_stride_b +
-                        (int64_t)i * p.o_stride_t + (int64_t)h * p.o_stride_h;
+  __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + o_off;
   if (mx == -INFINITY) {   // no key reached this row in any range
     for (int c = 0; c < C; ++c) orow[C * lane + c] = __float2bfloat16(0.f);
     if (p.lse != nullptr && lane == 0) p.lse[lse_row] = -INFINITY;
@@ -105,7 +114,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) splitkv_combine_kernel(con
 }  // namespace
 
 cudaError_t splitkv_combine_launch(const SplitCombineParams& p, int head_dim_v, cudaStream_t stream) {
-  const int64_t rows = (int64_t)p.batch * p.seqlen_q * p.heads_q;
+  const int64_t rows = (p.packed ? (int64_t)p.total_q : (int64_t)p.batch * p.seqlen_q) * p.heads_q;
   if (rows == 0) return cudaSuccess;
   const int64_t blocks = (rows + kCombineWarps - 1) / kCombineWarps;
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;

@@ -139,9 +139,11 @@ typedef struct attn_fwd_params {
 
   /* Split-KV: number of key ranges each query tile is split into (the
    * "splitk_partitions" of the SM100AttentionSMem page's configuration).
-   * 0 = chosen by the library (splits only non-causal fixed-length problems
-   * with too few query tiles to fill the GPU), 1 = off, n >= 2 = n ranges.
-   * Each range writes a normalised partial O and its LSE into the workspace
+   * 0 = chosen by the library (splits only unmasked problems with too few
+   * query tiles to fill the GPU), 1 = off, n >= 2 = n ranges (at most 64,
+   * capped at the key tiles of the longest sequence; a packed sequence with
+   * fewer key tiles leaves some of its ranges empty). Each range writes a
+   * normalised partial O and its LSE into the workspace
    * (attn_fwd_workspace_bytes grows accordingly) and a second small kernel
    * merges them. Causal problems do not split (UNSUPPORTED if n >= 2). */
   int32_t num_splits;
@@ -179,8 +181,8 @@ void attn_fwd_params_init(attn_fwd_params *p);
 size_t attn_fwd_params_size(void);
 
 /* Workspace bytes needed for `p`: ATTN_FWD_WORKSPACE_BYTES, plus with
- * split-KV (n ranges) the partial LSE, n*B*Hq*Sq floats rounded up to 256
- * bytes, and the partial O, n*B*Sq*Hq*Dv floats. The automatic split count
+ * split-KV (n ranges) the partial LSE, n*R*Hq floats rounded up to 256
+ * bytes, and the partial O, n*R*Hq*Dv floats (R = B*Sq, or Tq when packed). The automatic split count
  * (num_splits = 0) depends on the SM count of the current device: call this
  * with the device current that attn_fwd will run on. Never fails (an invalid
  * `p` or NULL gives ATTN_FWD_WORKSPACE_BYTES). */

@@ -205,22 +205,21 @@ def test_split_kv_automatic_choice(pkg):
     # A short-query / long-key problem with too few query tiles for the GPU splits ...
     auto = pkg.plan(_split_params(pkg)).num_splits
     assert 2 <= auto <= 64
-    # ... one with many query tiles, a causal one or a packed one does not.
+    # ... so does a packed one (from the bound B * ceil(max_len / 256) of its
+    # query tiles); one with many query tiles or a causal one does not.
+    assert pkg.plan(_split_params(pkg, packed=True)).num_splits == auto
     assert pkg.plan(_split_params(pkg, B=4, Sq=4096, Sk=4096, Hq=16, Hkv=16)).num_splits == 1
     assert pkg.plan(_split_params(pkg, causal=True)).num_splits == 1
-    assert pkg.plan(_split_params(pkg, packed=True)).num_splits == 1
     assert pkg.workspace_bytes(_split_params(pkg, causal=True)) == 256
     # a single key tile leaves nothing to split
     assert pkg.plan(_split_params(pkg, Sk=100)).num_splits == 1
 
 
-@pytest.mark.parametrize("case,status", [("causal", 2), ("packed", 2), ("simple", 2), ("too_many", 1),
+@pytest.mark.parametrize("case,status", [("causal", 2), ("simple", 2), ("too_many", 1),
                                          ("negative", 1), ("small_workspace", 1)])
 def test_split_kv_rejections(pkg, case, status):
     if case == "causal":
         p = _split_params(pkg, causal=True, splits=2)
-    elif case == "packed":
-        p = _split_params(pkg, packed=True, splits=2)
     elif case == "simple":
         p = _split_params(pkg, splits=2)
         p.backend = 1
@@ -320,3 +319,16 @@ def test_fp8_v_plan(pkg):
     info = pkg.plan(p)
     assert info.v_stages == 4 and info.k_stages == 4
     assert info.smem_bytes <= 232448
+
+
+def test_split_kv_packed_workspace_and_schedule(pkg):
+    p = _split_params(pkg, B=3, Sq=700, Sk=900, Hq=4, Hkv=2, splits=3, packed=True)
+    # packed: rows are the Tq = B * Sq rows of q
+    lse = (3 * 2100 * 4 * 4 + 255) // 256 * 256
+    assert pkg.workspace_bytes(p) == 256 + lse + 3 * 2100 * 4 * 128 * 4
+    lens = [700, 1, 300]
+    cu = [0, 700, 701, 1001]
+    order = pkg.schedule(p, host_cu_seqlens_q=cu, with_split=True)
+    expect = {(b, h, t, r) for b, n in enumerate(lens) for h in range(4) for t in range((n + 255) // 256)
+              for r in range(3)}
+    assert len(order) == len(expect) and set(order) == expect

@@ -22,6 +22,16 @@ CASES = {
     "rope_sk600_3": (S(1, 2, 2, 100, 600, 128, 128, False, seed=65, rope=64), 3),
     "fp8_sk900_4": (S(1, 2, 2, 130, 900, 128, 128, False, seed=66, qk_dtype="fp8"), 4),
     "d128_sq513_sk1025_7": (S(2, 2, 2, 513, 1025, 128, 128, False, seed=67), 7),
+    # packed sequences: each cut by its own key tiles; the 100-key sequence
+    # has one key tile, so three of its four ranges are empty
+    "packed_gqa_4": (S(3, 8, 2, 700, 1500, 128, 128, False, seed=69, lengths_q=(700, 1, 300),
+                       lengths_k=(1500, 100, 640)), 4),
+    "packed_d64_auto": (S(2, 4, 4, 256, 3000, 64, 64, False, seed=70, lengths_q=(256, 129),
+                          lengths_k=(3000, 2047)), 0),
+    "packed_fp8_3": (S(2, 4, 2, 300, 900, 128, 128, False, seed=71, qk_dtype="fp8", lengths_q=(300, 77),
+                       lengths_k=(900, 513)), 3),
+    "packed_rope_5": (S(2, 2, 2, 200, 800, 128, 128, False, seed=72, rope=64, lengths_q=(200, 130),
+                        lengths_k=(800, 129)), 5),
 }
 
 

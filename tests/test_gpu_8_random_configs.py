@@ -31,7 +31,7 @@ def _draw_case(seed):
         lk = lens if causal or not rng.integers(2) else [int(rng.integers(1, 600)) for _ in range(b)]
         spec = W.AttnSpec(b, hq, hkv, max(lens), max(lk), d, d, causal, seed=2000 + seed, lengths_q=tuple(lens),
                           lengths_k=tuple(lk), **kw)
-        splits = 1
+        splits = 1 if causal else int(rng.choice([0, 1, 3]))
     else:
         sq = lens[0]
         sk = sq if causal else int(rng.choice([sq, int(rng.integers(1, 1200))]))
