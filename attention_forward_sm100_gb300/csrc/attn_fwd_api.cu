@@ -63,15 +63,21 @@ attn_status validate(const attn_fwd_params* p) {
   if (!(p->softmax_scale > 0.f) || p->softmax_scale != p->softmax_scale)
     return fail(ATTN_ERR_INVALID_ARG, "softmax_scale must be a positive number");
   const bool packed = p->cu_seqlens_q != nullptr;
+  // K, V and the K rope part may be NULL only when there are no keys at all
+  // (an empty tensor has no storage); O is then 0 and LSE -inf.
+  const bool no_keys = packed ? p->total_k == 0 : p->seqlen_k == 0;
+  // Likewise Q and O without query rows (nothing is launched).
+  const bool no_queries = p->batch == 0 || (packed ? p->total_q == 0 : p->seqlen_q == 0);
   if (packed != (p->cu_seqlens_k != nullptr))
     return fail(ATTN_ERR_INVALID_ARG, "cu_seqlens_q and cu_seqlens_k must both be set or both NULL");
   if (packed && ((reinterpret_cast<uintptr_t>(p->cu_seqlens_q) | reinterpret_cast<uintptr_t>(p->cu_seqlens_k)) & 3))
     return fail(ATTN_ERR_INVALID_ARG, "cu_seqlens must be 4-byte aligned");
   if (packed && (p->total_q <= 0 && p->batch > 0 && p->seqlen_q > 0))
     return fail(ATTN_ERR_INVALID_ARG, "packed layout needs total_q");
-  if (p->q == nullptr || p->k == nullptr || p->v == nullptr || p->o == nullptr)
+  if ((!no_queries && (p->q == nullptr || p->o == nullptr)) ||
+      (!no_keys && !no_queries && (p->k == nullptr || p->v == nullptr)))
     return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be non-NULL");
-  if (p->rope_depth > 0 && (p->q_rope == nullptr || p->k_rope == nullptr))
+  if (p->rope_depth > 0 && !no_queries && (p->q_rope == nullptr || (!no_keys && p->k_rope == nullptr)))
     return fail(ATTN_ERR_INVALID_ARG, "rope_depth > 0 needs q_rope and k_rope");
   if (p->qk_dtype == ATTN_DTYPE_FP8_E4M3) {
     if (p->q_scale == nullptr || p->k_scale == nullptr)
@@ -249,7 +255,7 @@ attn_status make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt,
 // Depth-major fp8 V, [B][Hkv][Dv][Sk] with the keys contiguous: 4-D map over
 // (key, depth, head, batch); box {128 keys, Dv rows, 1, 1}, 128-byte swizzle,
 // so one box is the K-major B operand of the P.V product.
-attn_status make_map_vt(CUtensorMap* map, const attn_fwd_params* p) {
+attn_status make_map_vt(CUtensorMap* map, const attn_fwd_params* p, const void* base) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
   const int64_t sk = p->seqlen_k > 0 ? p->seqlen_k : 1;
@@ -261,7 +267,7 @@ attn_status make_map_vt(CUtensorMap* map, const attn_fwd_params* p) {
   cuuint64_t strides[3] = {(cuuint64_t)sd, (cuuint64_t)sh, (cuuint64_t)sb};
   cuuint32_t box[4] = {(cuuint32_t)af::kBlockN, (cuuint32_t)p->head_dim_v, 1u, 1u};
   cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(p->v), dims, strides, box, estr,
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(ATTN_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (%d) for fp8 V", (int)r);
@@ -283,12 +289,16 @@ attn_status launch_tc05(const attn_fwd_params* p, cudaStream_t stream) {
   if ((st = make_map(&prm.tm_q, p->q, qk_t, es, p->head_dim_qk, p->num_heads_q, tq, nb, p->q_stride[2],
                      p->q_stride[1], p->q_stride[0], box_qk)) != ATTN_OK)
     return st;
-  if ((st = make_map(&prm.tm_k, p->k, qk_t, es, p->head_dim_qk, p->num_heads_kv, tk, nb, p->k_stride[2],
+  // Without keys K and V are never read; their maps then point at Q.
+  const void* k_base = p->k != nullptr ? p->k : p->q;
+  const void* v_base = p->v != nullptr ? p->v : p->q;
+  const void* kr_base = p->k_rope != nullptr ? p->k_rope : p->q_rope;
+  if ((st = make_map(&prm.tm_k, k_base, qk_t, es, p->head_dim_qk, p->num_heads_kv, tk, nb, p->k_stride[2],
                      p->k_stride[1], p->k_stride[0], box_qk)) != ATTN_OK)
     return st;
   if (p->v_dtype == ATTN_DTYPE_FP8_E4M3) {
-    if ((st = make_map_vt(&prm.tm_v, p)) != ATTN_OK) return st;
-  } else if ((st = make_map(&prm.tm_v, p->v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->head_dim_v, p->num_heads_kv,
+    if ((st = make_map_vt(&prm.tm_v, p, v_base)) != ATTN_OK) return st;
+  } else if ((st = make_map(&prm.tm_v, v_base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->head_dim_v, p->num_heads_kv,
                             tk, nb, p->v_stride[2], p->v_stride[1], p->v_stride[0], 64)) != ATTN_OK) {
     return st;
   }
@@ -296,7 +306,7 @@ attn_status launch_tc05(const attn_fwd_params* p, cudaStream_t stream) {
     if ((st = make_map(&prm.tm_qr, p->q_rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->rope_depth, p->num_heads_q,
                        tq, nb, p->q_rope_stride[2], p->q_rope_stride[1], p->q_rope_stride[0], 64)) != ATTN_OK)
       return st;
-    if ((st = make_map(&prm.tm_kr, p->k_rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->rope_depth, 1, tk, nb,
+    if ((st = make_map(&prm.tm_kr, kr_base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->rope_depth, 1, tk, nb,
                        p->k_rope_stride[1], p->k_rope_stride[1], p->k_rope_stride[0], 64)) != ATTN_OK)
       return st;
   }

@@ -20,6 +20,8 @@ CASES = {
     "d128_noncausal_s513": S(1, 3, 3, 513, 513, 128, 128, False, seed=36),
     "d128_noncausal_sq200_sk333": S(2, 2, 1, 200, 333, 128, 128, False, seed=37),
     "d128_noncausal_sk1": S(1, 2, 2, 300, 1, 128, 128, False, seed=38),
+    "d128_noncausal_sk0": S(2, 2, 2, 130, 0, 128, 128, False, seed=52),
+    "fp8_noncausal_sk0": S(1, 2, 2, 70, 0, 128, 128, False, seed=53, qk_dtype="fp8"),
     "d128_causal_sq300_sk170": S(1, 2, 2, 300, 170, 128, 128, True, seed=39),
     "d64_causal_s1000": S(1, 2, 2, 1000, 1000, 64, 64, True, seed=40),
     "d64_gqa_noncausal_s390": S(2, 8, 2, 390, 390, 64, 64, False, seed=41),
@@ -124,3 +126,18 @@ def test_growing_scores_move_the_running_max(qk_dtype, causal):
     err = compare_full(inp)
     print(qk_dtype, causal, err)
     assert_within(err, qk_dtype)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("shape", [(0, 128, 2, 128), (2, 0, 2, 128)])
+def test_no_query_rows(shape):
+    """B = 0 or Sq = 0: nothing to compute, the call returns at once (Q and O
+    are empty tensors without storage)."""
+    import attention_forward_sm100_gb300 as pkg
+    q = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    kv_shape = (shape[0], 64, 2, 128)
+    k = torch.randn(kv_shape, device="cuda").to(torch.bfloat16)
+    v = torch.randn(kv_shape, device="cuda").to(torch.bfloat16)
+    o, lse = pkg.forward(q, k, v, causal=False)
+    pkg.check()
+    assert o.shape == shape and lse.numel() == 0
