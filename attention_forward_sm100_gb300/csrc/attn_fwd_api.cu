@@ -80,7 +80,7 @@ attn_status validate(const attn_fwd_params* p) {
   if (p->rope_depth > 0 && !no_queries && (p->q_rope == nullptr || (!no_keys && p->k_rope == nullptr)))
     return fail(ATTN_ERR_INVALID_ARG, "rope_depth > 0 needs q_rope and k_rope");
   if (p->qk_dtype == ATTN_DTYPE_FP8_E4M3) {
-    if (p->q_scale == nullptr || p->k_scale == nullptr)
+    if ((!no_queries && p->q_scale == nullptr) || (!no_keys && !no_queries && p->k_scale == nullptr))
       return fail(ATTN_ERR_INVALID_ARG, "fp8 Q/K need q_scale and k_scale");
     if (p->rope_depth > 0) return fail(ATTN_ERR_UNSUPPORTED, "fp8 Q/K with a rope part");
   }
