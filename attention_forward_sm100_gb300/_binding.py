@@ -108,19 +108,23 @@ def last_error() -> str:
 
 
 _workspaces = {}
+_workspaces_lock = threading.Lock()
 
 
 def default_workspace(device, nbytes: int = WORKSPACE_BYTES) -> torch.Tensor:
     """A zero-filled workspace per device of at least ``nbytes`` (the library
     keeps its counters zeroed; split-KV partial results need more room, so
-    the cached buffer is replaced by a larger one when a call asks for it)."""
+    the cached buffer is replaced by a larger one when a call asks for it).
+    Calls that use the default workspace must not overlap on the GPU (one
+    stream per device, or the caller's own workspaces)."""
     device = torch.device(device)
     key = (device.type, device.index)
-    ws = _workspaces.get(key)
-    if ws is None or ws.numel() < nbytes:
-        ws = torch.zeros(max(nbytes, WORKSPACE_BYTES), dtype=torch.uint8, device=device)
-        _workspaces[key] = ws
-    return ws
+    with _workspaces_lock:
+        ws = _workspaces.get(key)
+        if ws is None or ws.numel() < nbytes:
+            ws = torch.zeros(max(nbytes, WORKSPACE_BYTES), dtype=torch.uint8, device=device)
+            _workspaces[key] = ws
+        return ws
 
 
 def workspace_bytes(p: Params) -> int:
