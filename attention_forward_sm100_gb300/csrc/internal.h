@@ -12,6 +12,7 @@ constexpr int kRowsPerTile = 256;   // query rows per work tile of the tcgen05 k
 constexpr int kBlockM = 128;        // query rows per MMA tile (one TMEM lane per row)
 constexpr int kBlockN = 128;        // keys per K/V tile
 constexpr int64_t kL2ChunkBudget = 48ll << 20;   // K/V bytes one scheduling chunk may keep in L2
+constexpr int64_t kL2ChunkBudgetFp8 = 24ll << 20;   // the same for fp8 Q/K (measured best)
 constexpr int kMaxSplits = 64;      // split-KV ranges per query tile (the merge kernel holds 2 per lane)
 
 // Workspace words (uint32 each).
