@@ -6,29 +6,36 @@
 //   * a work tile is 256 query rows of one (sequence, head), split into two
 //     128-row Q tiles that ping-pong between two softmax warpgroups so the
 //     tensor core always has one Q tile's MMAs to run while the other tile's
-//     softmax runs;
+//     softmax runs (with split-KV, a work tile also names one range of the
+//     keys);
 //   * warp 14 is the scheduler and the Q/K producer: it takes work indices
-//     from an atomic counter, publishes each decoded work tile through a
-//     two-slot shared-memory ring (the shared work index of the scheduler
-//     page, initial_state / advance) and streams K tiles into a staged ring
-//     with TMA and transaction-count mbarriers (acquire / expect-bytes /
-//     commit of the producer-pipeline page); warp 15 streams V tiles into
-//     their own ring. K is stored k-major and V mn-major, both with the
-//     128-byte swizzle, exactly as the MMAs read them;
+//     from an atomic counter (or a static stride, or none: one CTA per work
+//     tile), publishes each decoded work tile through a two-slot
+//     shared-memory ring (the shared work index of the scheduler page,
+//     initial_state / advance) and streams K tiles into a staged ring with
+//     TMA and transaction-count mbarriers (acquire / expect-bytes / commit of
+//     the producer-pipeline page); warp 15 streams V tiles into their own
+//     ring. K is stored k-major and V mn-major (k-major when V is e4m3 and
+//     depth-major in memory), all with the 128-byte swizzle, exactly as the
+//     MMAs read them;
 //   * warps 12 and 13 each issue the tcgen05.mma of one Q tile from one
-//     thread: S_i = Q_i K^T into tensor memory (fp32), then O_i += P_i V with
-//     P_i (bf16) read from tensor memory where the softmax left it, over the
-//     S_i columns; one issuer per tile lets one tile's barrier waits overlap
-//     the other tile's MMAs;
+//     thread: per K/V step one group, O_i += P_i V (P_i read from tensor
+//     memory where the softmax left it, over the S_i columns) then
+//     S_i = Q_i K^T into tensor memory (fp32); the two issuers' groups
+//     strictly alternate through a turn token (the forced-ordering barriers
+//     of the layout page);
 //   * warpgroups 0 and 1 own Q tiles 0 and 1: thread r owns row r (TMEM lane
 //     r), loads S, applies the causal / sequence-end mask, keeps the running
-//     max m and sum l in log2 units, writes P = 2^(s*c - m) as bf16 back to
-//     tensor memory and passes the rescale factor alpha through shared
-//     memory (the correction region of the layout page). The running max is
-//     only moved when it grows by more than 2^8, so most tiles need no
-//     rescale; O and l stay consistent because both use the same max;
-//   * warpgroup 2 rescales O_i in tensor memory when alpha != 1 and, after
-//     the last P V, normalises O by 1/l, rounds once to bf16 and stores it.
+//     max m and sum l in log2 units and writes P = 2^(s*c - m) (bf16, or
+//     e4m3 for an e4m3 V) back to tensor memory in two halves. The running
+//     max only moves when it grows by more than 2^8, so most tiles need no
+//     rescale; when it moves, the softmax warp rescales its own rows of O_i
+//     in tensor memory before publishing P. O and l share the max, so O/l is
+//     exact;
+//   * warpgroup 2 is the epilogue: after the last P V it normalises O by 1/l
+//     (handed over through shared memory, the correction region of the
+//     layout page), rounds once to bf16 and stores it, or stores the fp32
+//     partial row of a split-KV range.
 // Every wait is bounded: on timeout the CTA records an error in the
 // workspace, raises a shared abort flag that all waits poll, drains its
 // outstanding copies and MMAs, frees tensor memory and exits.
