@@ -1,5 +1,7 @@
 // Host side of the C ABI declared in include/attn_fwd.h: argument validation,
-// launch planning, TMA descriptor encoding and kernel dispatch.
+// launch planning (grid, split-KV count, workspace layout), TMA descriptor
+// encoding and kernel dispatch (the attention kernel, then the split-KV
+// merge when the keys are split).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdarg.h>

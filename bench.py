@@ -1,10 +1,12 @@
 """Throughput of the fused attention forward on GB300.
 
 One step = one attn_fwd call (the whole hot path: scheduling, TMA loads,
-QK^T, softmax, correction, PV and the epilogue) over the chosen workload,
-inputs resident in HBM. Prints one JSON line on rank 0.
+QK^T, softmax, correction, PV and the epilogue, plus the split-KV merge when
+the workload splits) over the chosen workload, inputs resident in HBM.
+Prints one JSON line on rank 0.
 
   python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl ours|reference]
+                  [--schedule dynamic|static|grid]
 
 Multi-GPU (torchrun): every rank runs an independent replica of the workload
 (weak scaling, no collective on the data path); value = FLOPs of all ranks /
