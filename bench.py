@@ -228,6 +228,8 @@ def dist_setup(args):
     if world > 1:
         import torch.distributed as dist
         backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)   # this rank's GPU before any NCCL communicator exists
         dist.init_process_group(backend)
     return world, rank, local
 
