@@ -48,6 +48,29 @@ __global__ void __launch_bounds__(kCombineWarps * 32) splitkv_combine_kernel(con
     o_off = (int64_t)b * p.o_stride_b + (int64_t)i * p.o_stride_t + (int64_t)h * p.o_stride_h;
   }
   const int64_t lse_split = qrows * p.heads_q;
+  const int64_t o_split = rows * DV;
+  const float* src = p.o_part + row * DV + C * lane;
+  // Ranges in batches of kBatch: a batch's loads are all issued before any
+  // is used, and the first batch is issued before the weights are worked
+  // out (the partial rows do not depend on them), so each warp keeps its
+  // row reads in flight across the LSE reduction.
+  float v[kBatch][C];
+  auto load_batch = [&](int s0) {
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (s0 + u < p.splits) {
+        const float* x = src + (int64_t)(s0 + u) * o_split;
+        if constexpr (C == 4) {
+          const float4 t4 = __ldcs(reinterpret_cast<const float4*>(x));
+          v[u][0] = t4.x; v[u][1] = t4.y; v[u][2] = t4.z; v[u][3] = t4.w;
+        } else {
+          const float2 t2 = __ldcs(reinterpret_cast<const float2*>(x));
+          v[u][0] = t2.x; v[u][1] = t2.y;
+        }
+      }
+    }
+  };
+  load_batch(0);
   float l0 = -INFINITY, l1 = -INFINITY;
   if (lane < p.splits) l0 = p.lse_part[lane * lse_split + lse_row];
   if (lane + 32 < p.splits) l1 = p.lse_part[(lane + 32) * lse_split + lse_row];
@@ -70,25 +93,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) splitkv_combine_kernel(con
   float acc[C];
 #pragma unroll
   for (int c = 0; c < C; ++c) acc[c] = 0.f;
-  const int64_t o_split = rows * DV;
-  const float* src = p.o_part + row * DV + C * lane;
-  // Ranges in batches of kBatch: the batch's loads are all issued before any
-  // is used, so each warp keeps kBatch row reads in flight.
   for (int s0 = 0; s0 < p.splits; s0 += kBatch) {
-    float v[kBatch][C];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      if (s0 + u < p.splits) {
-        const float* x = src + (int64_t)(s0 + u) * o_split;
-        if constexpr (C == 4) {
-          const float4 t = __ldcs(reinterpret_cast<const float4*>(x));
-          v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
-        } else {
-          const float2 t = __ldcs(reinterpret_cast<const float2*>(x));
-          v[u][0] = t.x; v[u][1] = t.y;
-        }
-      }
-    }
+    if (s0 > 0) load_batch(s0);
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int s = s0 + u;
