@@ -22,7 +22,10 @@
  *
  * Conventions
  *   - Every pointer in attn_fwd_params is a DEVICE pointer owned by the caller.
- *     The library allocates no memory and keeps no mutable global state.
+ *     The library allocates no memory. Its only process-wide state is
+ *     read-mostly caches (the SM count per device, the driver's tensor-map
+ *     encoder entry point) and the fixed scratch array of attn_fwd_noalloc;
+ *     calls on different workspaces and streams are independent.
  *   - attn_fwd() validates, encodes TMA descriptors on the host and enqueues
  *     one kernel on `stream` (two with split-KV: the partial ranges, then
  *     their merge); it returns without synchronising. Invalid
