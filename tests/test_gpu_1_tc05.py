@@ -141,3 +141,43 @@ def test_no_query_rows(shape):
     o, lse = pkg.forward(q, k, v, causal=False)
     pkg.check()
     assert o.shape == shape and lse.numel() == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("packed", [False, True])
+def test_strided_views_of_fused_buffers(packed):
+    """Q, K and V as views into one fused [.., 3, H, D] projection buffer
+    (token stride 3*H*D), the rope parts likewise, and O written into a wider
+    buffer (token stride 2*H*Dv): the kernel follows the strides it is given
+    and leaves the rest of the output buffer alone."""
+    import attention_forward_sm100_gb300 as pkg
+    from helpers import errors, f64, run_oracle, TOL
+    lens = (300, 129) if packed else None
+    spec = S(2, 4, 4, 300, 300, 128, 128, True, seed=54, rope=64, lengths_q=lens)
+    inp = W.make_inputs(spec)
+    dev = torch.device("cuda")
+    lead = inp["q"].shape[:-2]                                   # (B, S) or (T,)
+    fused = torch.zeros(lead + (3, 4, 128), dtype=torch.bfloat16)
+    for n, slot in (("q", 0), ("k", 1), ("v", 2)):
+        fused[..., slot, :, :] = inp[n]
+    fused_r = torch.zeros(lead + (2, 4, 64), dtype=torch.bfloat16)
+    fused_r[..., 0, :, :] = inp["q_rope"]
+    fused = fused.to(dev)
+    fused_r = fused_r.to(dev)
+    q, k, v = fused[..., 0, :, :], fused[..., 1, :, :], fused[..., 2, :, :]
+    q_rope = fused_r[..., 0, :, :]
+    k_rope = inp["k_rope"].to(dev)
+    out_buf = torch.full(lead + (2, 4, 128), 7.0, dtype=torch.bfloat16, device=dev)
+    o = out_buf[..., 1, :, :]
+    assert q.stride()[-3] == 3 * 4 * 128 and o.stride()[-3] == 2 * 4 * 128
+    lq, lk = spec.seq_lengths()
+    cu = {n: (inp[n].to(dev) if inp.get(n) is not None else None) for n in ("cu_seqlens_q", "cu_seqlens_k")}
+    _, lse = pkg.forward(q, k, v, causal=True, softmax_scale=spec.softmax_scale, q_rope=q_rope, k_rope=k_rope,
+                         cu_seqlens_q=cu["cu_seqlens_q"], cu_seqlens_k=cu["cu_seqlens_k"],
+                         max_seqlen_q=max(lq), max_seqlen_k=max(lk), out=o)
+    pkg.check()
+    o_ref, lse_ref = run_oracle(inp)
+    err = errors(f64(o.cpu()), o_ref, lse.cpu().double().numpy(), lse_ref)
+    for key, bound in TOL["bf16"].items():
+        assert err[key] <= bound, err
+    assert bool((out_buf[..., 0, :, :] == 7.0).all())            # the other half is untouched
