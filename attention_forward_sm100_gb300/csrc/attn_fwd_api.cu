@@ -96,7 +96,7 @@ attn_status validate(const attn_fwd_params* p) {
   }
   for (int i = 0; i < 3; ++i) {
     if (p->q_stride[i] < 0 || p->k_stride[i] < 0 || p->v_stride[i] < 0 || p->o_stride[i] < 0 ||
-        p->q_rope_stride[i] < 0)
+        p->q_rope_stride[i] < 0 || (i < 2 && p->k_rope_stride[i] < 0))
       return fail(ATTN_ERR_INVALID_ARG, "negative stride");
   }
   if (p->backend == ATTN_BACKEND_TCGEN05) {
@@ -122,7 +122,10 @@ attn_status validate(const attn_fwd_params* p) {
       for (int i = packed ? 1 : 0; i < 2; ++i)
         if ((p->k_rope_stride[i] * 2) % 16) return fail(ATTN_ERR_INVALID_ARG, "k_rope strides must be multiples of 16 bytes");
     }
-    if ((p->o_stride[2] * 2) % 16 || (p->o_stride[1] * 2) % 16 || !aligned16(p->o))
+    // The epilogue stores whole rows in 16-byte pieces, so every stride that
+    // moves between rows (batch too, unless packed) must keep that alignment.
+    if ((p->o_stride[2] * 2) % 16 || (p->o_stride[1] * 2) % 16 || (!packed && (p->o_stride[0] * 2) % 16) ||
+        !aligned16(p->o))
       return fail(ATTN_ERR_INVALID_ARG, "o must be 16-byte aligned with 16-byte multiple strides");
     const bool ok_bf16 = p->qk_dtype == ATTN_DTYPE_BF16 &&
         ((p->head_dim_qk == 64 && p->head_dim_v == 64 && p->rope_depth == 0) ||
@@ -433,6 +436,9 @@ attn_status attn_fwd_check(void* workspace, attn_stream_t stream) {
     const uint32_t info = w[af::kWsErrorInfo];
     cudaMemset(static_cast<uint32_t*>(workspace) + af::kWsErrorCode, 0, 2 * sizeof(uint32_t));
     cudaDeviceSynchronize();
+    if (w[af::kWsErrorCode] == af::kDevErrBadSeqlens)
+      return fail(ATTN_ERR_INVALID_ARG, "cu_seqlens of sequence %u are decreasing or exceed total_q / total_k "
+                  "(nothing of that call's output can be trusted)", info);
     return fail(ATTN_ERR_DEVICE_TIMEOUT, "device wait timed out (code %u, block %u, role %u, barrier %u)",
                 w[af::kWsErrorCode], info >> 16, (info >> 8) & 0xffu, info & 0xffu);
   }

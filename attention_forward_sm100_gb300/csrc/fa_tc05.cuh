@@ -289,7 +289,22 @@ __device__ __forceinline__ SchedSlot decode_work(const Tc05Params& P, int64_t w,
   while (true) {
     const int bb = cur.b + lane;
     int64_t u = 0;
-    if (bb < P.batch) u = (int64_t)tiles_for(P.cu_q[bb + 1] - P.cu_q[bb], kRowsPerTile) * P.heads_q * P.num_splits;
+    bool bad = false;
+    if (bb < P.batch) {
+      // Offsets that would index outside q/k/v/o are refused here, before
+      // any use: every sequence passes through this scan in some CTA (the
+      // one whose work index runs past the batch scans to its end).
+      const int qs = P.cu_q[bb], qe = P.cu_q[bb + 1], ks = P.cu_k[bb], ke = P.cu_k[bb + 1];
+      bad = qs < 0 || qe < qs || qe > P.total_q || ks < 0 || ke < ks || ke > P.total_k;
+      if (!bad) u = (int64_t)tiles_for(qe - qs, kRowsPerTile) * P.heads_q * P.num_splits;
+    }
+    const unsigned bad_lanes = __ballot_sync(kFull, bad);
+    if (bad_lanes) {
+      // record it and end this CTA's work (its roles see an invalid slot)
+      if (lane == 0 && atomicCAS(&P.ws[kWsErrorCode], 0u, (uint32_t)kDevErrBadSeqlens) == 0u)
+        atomicExch(&P.ws[kWsErrorInfo], (uint32_t)(cur.b + __ffs(bad_lanes) - 1));
+      return s;
+    }
     int64_t incl = u;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {

@@ -28,6 +28,7 @@ enum WorkspaceWord : int {
 enum DeviceError : uint32_t {
   kDevErrNone = 0,
   kDevErrTimeout = 1,
+  kDevErrBadSeqlens = 3,   // packed offsets out of order or past total_q / total_k (info: sequence)
 };
 
 // Everything the tcgen05 kernel needs, passed as one __grid_constant__ struct.

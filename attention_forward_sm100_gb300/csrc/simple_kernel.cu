@@ -37,6 +37,10 @@ __global__ void __launch_bounds__(kWarps * 32) simple_attn_kernel(const attn_fwd
     lq = p.cu_seqlens_q[b + 1] - p.cu_seqlens_q[b];
     k_base_tok = p.cu_seqlens_k[b];
     lk = p.cu_seqlens_k[b + 1] - p.cu_seqlens_k[b];
+    // offsets outside q/k/v/o: leave the sequence alone (cross-check kernel only)
+    if (q_base_tok < 0 || lq < 0 || q_base_tok + lq > p.total_q || k_base_tok < 0 || lk < 0 ||
+        k_base_tok + lk > p.total_k)
+      return;
   }
   if (i >= lq) return;
   const int hk = h / (p.num_heads_q / p.num_heads_kv);

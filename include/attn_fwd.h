@@ -213,8 +213,11 @@ attn_status attn_fwd(const attn_fwd_params *p, attn_stream_t stream);
 attn_status attn_fwd_noalloc(const attn_fwd_params *p, attn_stream_t stream);
 
 /* Synchronises `stream`, reads and clears the device error record of
- * `workspace`. Returns DEVICE_TIMEOUT if a kernel wait ran out, CUDA for a
- * pending CUDA error, else OK. */
+ * `workspace`. Returns DEVICE_TIMEOUT if a kernel wait ran out, INVALID_ARG
+ * if the kernel found packed offsets (cu_seqlens) decreasing or past
+ * total_q / total_k (it then skipped that work and wrote nothing outside
+ * the tensors; the call's output cannot be trusted), CUDA for a pending CUDA
+ * error, else OK. */
 attn_status attn_fwd_check(void *workspace, attn_stream_t stream);
 
 /* Validates `p` and reports the launch plan without touching the GPU,
