@@ -332,3 +332,16 @@ def test_split_kv_packed_workspace_and_schedule(pkg):
     expect = {(b, h, t, r) for b, n in enumerate(lens) for h in range(4) for t in range((n + 255) // 256)
               for r in range(3)}
     assert len(order) == len(expect) and set(order) == expect
+
+
+def test_output_batch_stride_alignment(pkg):
+    """The epilogue stores 16-byte pieces of each O row, so O's batch stride
+    must be a multiple of 8 bf16 elements as well (fixed-length layout)."""
+    q = _Fake((2, 300, 4, 128), ptr=1 << 20)
+    ws = _Fake((256,), dtype=torch.uint8, ptr=5 << 20)
+    good = _Fake((2, 300, 4, 128), ptr=4 << 20)
+    bad = _Fake((2, 300, 4, 128), ptr=4 << 20, strides=(300 * 4 * 128 + 4, 4 * 128, 128, 1))
+    pkg.plan(pkg.make_params(q, q, q, causal=True, out=good, lse=None, workspace=ws))
+    with pytest.raises(pkg.AttnError) as e:
+        pkg.plan(pkg.make_params(q, q, q, causal=True, out=bad, lse=None, workspace=ws))
+    assert e.value.status == 1 and "o must be" in str(e.value)
