@@ -147,11 +147,62 @@ def head_dim_v(v) -> int:
     return v.shape[-2] if v.dtype == torch.float8_e4m3fn else v.shape[-1]
 
 
+def _check_layout(q, k, v, packed, out=None, lse=None, q_rope=None, k_rope=None, q_scale=None, k_scale=None,
+                  cu_seqlens_q=None, cu_seqlens_k=None):
+    """Shapes (and, for the tensors passed as bare pointers, contiguity) that
+    the library's sizes are derived from; a mismatch would make it read or
+    write outside a tensor, so it is refused here."""
+    def shape(t):
+        return tuple(t.shape)
+
+    def need(cond, msg):
+        if not cond:
+            raise ValueError(msg)
+
+    v_fp8 = v.dtype == torch.float8_e4m3fn
+    if packed:
+        need(len(shape(q)) == 3 and len(shape(k)) == 3, "packed q and k must be [T, H, D]")
+        tq, hq, d = shape(q)
+        tk, hkv, dk = shape(k)
+        b = shape(cu_seqlens_q)[0] - 1
+        need(shape(cu_seqlens_k) == (b + 1,), "cu_seqlens_k must have the length of cu_seqlens_q")
+        dv = shape(v)[1] if v_fp8 else shape(v)[-1]
+        need(shape(v) == ((hkv, dv, tk) if v_fp8 else (tk, hkv, dv)), f"v shape {shape(v)} does not match k")
+        o_shape, lse_shape = (tq, hq, dv), (hq, tq)
+        qs_shape, ks_shape, kr_lead = (hq, tq), (hkv, tk), (tk,)
+    else:
+        need(len(shape(q)) == 4 and len(shape(k)) == 4, "q and k must be [B, S, H, D]")
+        b, sq, hq, d = shape(q)
+        bk, sk, hkv, dk = shape(k)
+        need(bk == b, "q and k batch sizes differ")
+        dv = shape(v)[2] if v_fp8 else shape(v)[-1]
+        need(shape(v) == ((b, hkv, dv, sk) if v_fp8 else (b, sk, hkv, dv)), f"v shape {shape(v)} does not match k")
+        o_shape, lse_shape = (b, sq, hq, dv), (b, hq, sq)
+        qs_shape, ks_shape, kr_lead = (b, hq, sq), (b, hkv, sk), (b, sk)
+    need(dk == d, "q and k depths differ")
+    if out is not None:
+        need(shape(out) == o_shape, f"out shape {shape(out)} != {o_shape}")
+    for name, t, want in (("lse", lse, lse_shape), ("q_scale", q_scale, qs_shape), ("k_scale", k_scale, ks_shape)):
+        if t is not None:
+            need(shape(t) == want, f"{name} shape {shape(t)} != {want}")
+            if isinstance(t, torch.Tensor):
+                need(t.is_contiguous(), f"{name} must be contiguous")
+    if q_rope is not None:
+        r = shape(q_rope)[-1]
+        need(shape(q_rope) == shape(q)[:-1] + (r,), "q_rope must match q but for its depth")
+        need(k_rope is not None and shape(k_rope) == kr_lead + (r,), f"k_rope must be {kr_lead + (r,)}")
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if isinstance(t, torch.Tensor):
+            need(t.is_contiguous() and t.dtype == torch.int32, f"{name} must be a contiguous int32 tensor")
+
+
 def make_params(q, k, v, *, causal, softmax_scale=None, q_rope=None, k_rope=None, q_scale=None, k_scale=None,
                 cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, out=None, lse=None,
                 workspace=None, backend="tcgen05", num_splits=0, schedule="dynamic") -> Params:
     """attn_fwd_params for torch tensors (shapes are read, nothing is allocated)."""
     packed = cu_seqlens_q is not None
+    _check_layout(q, k, v, packed, out=out, lse=lse, q_rope=q_rope, k_rope=k_rope, q_scale=q_scale,
+                  k_scale=k_scale, cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k)
     p = Params()
     if packed:
         tq, hq, d = q.shape

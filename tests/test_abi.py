@@ -291,7 +291,8 @@ def test_fp8_v_rejections(pkg, case, status):
     k = _Fake((1, sk, 4, 128), dtype=qdt, ptr=2 << 20)
     v = _Fake((1, 4, dv, sk), dtype=f8, ptr=3 << 20)
     o = _Fake((1, 256, 4, dv), ptr=4 << 20)
-    sc = _Fake((1, 4, 256), dtype=torch.float32, ptr=6 << 20)
+    qsc = _Fake((1, 4, 256), dtype=torch.float32, ptr=6 << 20)
+    ksc = _Fake((1, 4, sk), dtype=torch.float32, ptr=9 << 20)
     ws = _Fake((256,), dtype=torch.uint8, ptr=5 << 20)
     kw = {}
     if case == "packed":
@@ -299,8 +300,10 @@ def test_fp8_v_rejections(pkg, case, status):
         k = _Fake((sk, 4, 128), dtype=f8, ptr=2 << 20)
         v = _Fake((4, dv, sk), dtype=f8, ptr=3 << 20)
         o = _Fake((256, 4, dv), ptr=4 << 20)
+        qsc = _Fake((4, 256), dtype=torch.float32, ptr=6 << 20)
+        ksc = _Fake((4, sk), dtype=torch.float32, ptr=9 << 20)
         kw = dict(cu_seqlens_q=_Fake((2,), ptr=7 << 20), cu_seqlens_k=_Fake((2,), ptr=8 << 20))
-    p = pkg.make_params(q, k, v, causal=True, out=o, lse=None, workspace=ws, q_scale=sc, k_scale=sc, **kw)
+    p = pkg.make_params(q, k, v, causal=True, out=o, lse=None, workspace=ws, q_scale=qsc, k_scale=ksc, **kw)
     assert p.v_dtype == 1 and p.head_dim_v == dv
     with pytest.raises(pkg.AttnError) as e:
         pkg.plan(p)
@@ -345,3 +348,33 @@ def test_output_batch_stride_alignment(pkg):
     with pytest.raises(pkg.AttnError) as e:
         pkg.plan(pkg.make_params(q, q, q, causal=True, out=bad, lse=None, workspace=ws))
     assert e.value.status == 1 and "o must be" in str(e.value)
+
+
+@pytest.mark.parametrize("case", ["v_len", "v_heads", "out", "lse", "k_scale", "k_rope", "noncontig_lse", "cu_dtype"])
+def test_binding_refuses_inconsistent_shapes(pkg, case):
+    """The library derives every extent from q and k; the binding refuses
+    tensors whose shapes disagree with them before building the call."""
+    m = lambda *s, dt=torch.bfloat16: torch.empty(s, dtype=dt, device="meta")  # noqa: E731
+    q, k, v = m(2, 64, 4, 128), m(2, 80, 2, 128), m(2, 80, 2, 128)
+    kw = {}
+    if case == "v_len":
+        v = m(2, 79, 2, 128)
+    elif case == "v_heads":
+        v = m(2, 80, 4, 128)
+    elif case == "out":
+        kw["out"] = m(2, 64, 4, 64)
+    elif case == "lse":
+        kw["lse"] = m(2, 64, 4, dt=torch.float32)
+    elif case == "k_scale":
+        q8, k8 = m(2, 64, 4, 128, dt=torch.float8_e4m3fn), m(2, 80, 2, 128, dt=torch.float8_e4m3fn)
+        q, k = q8, k8
+        kw.update(q_scale=m(2, 4, 64, dt=torch.float32), k_scale=m(2, 2, 64, dt=torch.float32))
+    elif case == "k_rope":
+        kw.update(q_rope=m(2, 64, 4, 64), k_rope=m(2, 80, 32))
+    elif case == "noncontig_lse":
+        kw["lse"] = m(2, 64, 4, dt=torch.float32).permute(0, 2, 1)
+    else:
+        q, k, v = m(100, 4, 128), m(120, 2, 128), m(120, 2, 128)
+        kw.update(cu_seqlens_q=m(3, dt=torch.int64), cu_seqlens_k=m(3, dt=torch.int64))
+    with pytest.raises(ValueError):
+        pkg.make_params(q, k, v, causal=False, **kw)
