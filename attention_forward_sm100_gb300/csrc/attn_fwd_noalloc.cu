@@ -12,9 +12,12 @@
 // The array is a file-scope __device__ variable, so every GPU that loads the
 // library holds its own copy until the process exits. Host code cannot use
 // the array's name as a device address; its device address is looked up with
-// cudaGetSymbolAddress once per device, the first time this entry point runs
-// on that device (with that device current). Make that first call before any
-// stream capture begins.
+// cudaGetSymbolAddress (with the device current). The first call on a device
+// does that set-up; make it before any stream capture begins. Later calls
+// look the address up again whenever their stream is not capturing (the
+// lookup allocates nothing), so a context that was torn down and recreated
+// (cudaDeviceReset) never receives a stale address; while a capture is
+// running they reuse the address found before it.
 #include <cuda_runtime.h>
 #include <stdio.h>
 
@@ -33,15 +36,24 @@ constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 void* g_workspace_ptr[kMaxDevices] = {};
 
-// Device address of this device's copy of the array (looked up once).
-attn_status static_workspace(void** out) {
+// Device address of the current device's copy of the array: looked up again
+// on every call made outside a stream capture, reused from the last lookup
+// inside one.
+attn_status static_workspace(cudaStream_t stream, void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return af::report_error(ATTN_ERR_CUDA, "cudaGetDevice failed: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices)
     return af::report_error(ATTN_ERR_UNSUPPORTED, "device index %d beyond the %d devices supported", dev, kMaxDevices);
+  cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(stream, &capture);
+  if (e != cudaSuccess)
+    return af::report_error(ATTN_ERR_CUDA, "cudaStreamIsCapturing failed: %s", cudaGetErrorString(e));
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (g_workspace_ptr[dev] == nullptr) {
+  if (capture != cudaStreamCaptureStatusNone && g_workspace_ptr[dev] == nullptr)
+    return af::report_error(ATTN_ERR_INVALID_ARG, "the first attn_fwd_noalloc call on a device must come before "
+                            "any stream capture (it looks up the static workspace's address)");
+  if (capture == cudaStreamCaptureStatusNone) {
     void* ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, g_static_workspace);
     if (e != cudaSuccess || ptr == nullptr)
@@ -68,7 +80,7 @@ extern "C" attn_status attn_fwd_noalloc(const attn_fwd_params* p, attn_stream_t 
                             "this call needs %zu bytes of scratch, more than the %zu-byte static workspace", need,
                             kStaticWorkspaceBytes);
   void* ws = nullptr;
-  attn_status st = static_workspace(&ws);
+  attn_status st = static_workspace(reinterpret_cast<cudaStream_t>(stream), &ws);
   if (st != ATTN_OK) return st;
   q.workspace = ws;
   q.workspace_bytes = kStaticWorkspaceBytes;

@@ -6,7 +6,13 @@ the workload splits) over the chosen workload, inputs resident in HBM.
 Prints one JSON line on rank 0.
 
   python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl ours|reference]
-                  [--schedule dynamic|static|grid]
+                  [--schedule dynamic|static|grid] [--no-workloads]
+
+After the headline workload (its JSON keys: value, roofline, e2e, clocks,
+cpu_baseline), a one-GPU run also times every other workload the same way
+(warm-up, K calls under CUDA events, clocks sampled) and reports each under
+"workloads": kernel time, TFLOP/s and the fraction of the measured peak of
+its own MMA types.
 
 Multi-GPU (torchrun): every rank runs an independent replica of the workload
 (weak scaling, no collective on the data path); value = FLOPs of all ranks /
@@ -73,7 +79,9 @@ def parse_args():
     ap.add_argument("--schedule", default="dynamic", choices=["dynamic", "static", "grid"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip timing the other task workloads after the headline one")
     return ap.parse_args()
 
 
@@ -255,6 +263,117 @@ def barrier(world):
         dist.barrier()
 
 
+# The task's workloads timed after the headline one in the same run (GPU
+# only, no CPU leg): the small non-causal case, packed GQA, MLA with the
+# shared rope part and FP8 Q/K; then the two additions (all-FP8 and split-KV).
+OTHER_WORKLOADS = ("mha_b1_h2_s128_d64_noncausal", "varlen_gqa_b8_hq32_hkv8_d128_causal",
+                   "mla_b2_h128_s4096_d128r64_causal", "fp8_b2_h32_s8192_d128_causal",
+                   "fp8qkv_b2_h32_s8192_d128_causal", "splitkv_b1_hq32_hkv8_sq256_sk32768_d128_noncausal")
+
+
+def prepare(spec, dev, schedule):
+    """Device inputs, outputs and the keyword arguments of pkg.forward for a
+    workload; also the split count the library chose and kernels per call."""
+    import torch
+
+    import attention_forward_sm100_gb300 as pkg
+    from attention_forward_sm100_gb300 import workloads as W
+    inputs = W.make_inputs(spec)
+    d = W.to_device(inputs, dev)
+    lq, lk = spec.seq_lengths()
+    out = torch.empty(d["q"].shape[:-1] + (spec.d_v,), dtype=torch.bfloat16, device=dev)
+    if spec.varlen:
+        lse = torch.empty((spec.heads_q, d["q"].shape[0]), dtype=torch.float32, device=dev)
+    else:
+        lse = torch.empty((spec.batch, spec.heads_q, spec.seqlen_q), dtype=torch.float32, device=dev)
+    kw = dict(causal=spec.causal, softmax_scale=spec.softmax_scale, q_rope=d.get("q_rope"), k_rope=d.get("k_rope"),
+              q_scale=d.get("q_scale"), k_scale=d.get("k_scale"), cu_seqlens_q=d.get("cu_seqlens_q"),
+              cu_seqlens_k=d.get("cu_seqlens_k"), max_seqlen_q=max(lq), max_seqlen_k=max(lk), out=out, lse=lse,
+              schedule=schedule)
+    prm = pkg.make_params(d["q"], d["k"], d["v"], **kw)
+    ws = pkg.default_workspace(dev, pkg.workspace_bytes(prm))
+    prm.workspace, prm.workspace_bytes = ws.data_ptr(), ws.numel()
+    num_splits = pkg.plan(prm).num_splits
+    return inputs, d, kw, out, lse, num_splits, (2 if num_splits > 1 else 1)
+
+
+def time_calls(step, steps, stream):
+    """Per-call device times (ms) of `steps` calls, CUDA events on `stream`."""
+    import torch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record(stream)
+    for i in range(steps):
+        step()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)], ev[0].elapsed_time(ev[-1])
+
+
+def soak(step, dev, seconds):
+    """Keeps the same calls running so the clock sampler sees them."""
+    import torch
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        for _ in range(16):
+            step()
+        torch.cuda.synchronize(dev)
+
+
+def peak_label(spec, peak_src):
+    if spec.v_dtype == "fp8":
+        return f"2 x bf16 burst (fp8 Q/K/V), {peak_src}"
+    if spec.qk_dtype == "fp8":
+        return f"blended: half the FLOPs at 2 x bf16 burst (fp8 QK^T), half at bf16 burst, {peak_src}"
+    return f"bf16 burst, {peak_src}"
+
+
+def time_other_workloads(args, dev, stream, peaks, peak_src):
+    """kernel_ms, TFLOP/s, fraction of the measured peak of the workload's
+    own MMA types and clocks of every other workload, each timed like the
+    headline one."""
+    import torch
+
+    import attention_forward_sm100_gb300 as pkg
+    from attention_forward_sm100_gb300 import workloads as W
+    res = {}
+    for name in OTHER_WORKLOADS:
+        if name == args.workload:
+            continue
+        spec = W.WORKLOADS[name]
+        inputs, d, kw, out, lse, splits, launches = prepare(spec, dev, args.schedule)
+
+        def step():
+            pkg.forward(d["q"], d["k"], d["v"], stream=stream, **kw)
+
+        for _ in range(max(3, args.warmup)):
+            step()
+        pkg.check(device=dev)
+        clocks = ClockSampler(dev.index if dev.index is not None else 0)
+        clocks.start()
+        time.sleep(0.2)
+        torch.cuda.synchronize(dev)
+        per_call, _ = time_calls(step, args.steps, stream)
+        soak(step, dev, 0.6)
+        clk = clocks.stop()
+        pkg.check(device=dev)
+        kernel_ms = statistics.mean(per_call)
+        flops = spec.flops()
+        peak = peak_tflops(spec, peaks)
+        achieved = flops / (kernel_ms * 1e-3) / 1e12
+        entry = {"kernel_ms": kernel_ms, "median_ms": statistics.median(per_call), "tflops": achieved,
+                 "frac": achieved / peak, "peak": peak, "peak_source": peak_label(spec, peak_src),
+                 "flops_per_call": flops, "hbm_bytes_algorithmic": spec.hbm_bytes(), "num_splits": splits,
+                 "gpu_launches": args.steps * launches, "steps": args.steps, "clocks": clk}
+        if flops < 1e10:
+            med = statistics.median(per_call)
+            entry["us_per_call"] = med * 1e3
+            entry["algorithmic_gbs"] = spec.hbm_bytes() / (med * 1e-3) / 1e9
+        res[name] = entry
+        del inputs, d, kw, out, lse
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_reference(args, spec, world, rank):
     """Reference arm: the CPU oracle as it stands, one bounded sample of the
     workload per step. Under torchrun only rank 0 runs and prints."""
@@ -302,27 +421,11 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     pkg.lib()
-    inputs = W.make_inputs(spec)
-    d = W.to_device(inputs, dev)
-    lq, lk = spec.seq_lengths()
-    out = torch.empty(d["q"].shape[:-1] + (spec.d_v,), dtype=torch.bfloat16, device=dev)
-    if spec.varlen:
-        lse = torch.empty((spec.heads_q, d["q"].shape[0]), dtype=torch.float32, device=dev)
-    else:
-        lse = torch.empty((spec.batch, spec.heads_q, spec.seqlen_q), dtype=torch.float32, device=dev)
-    kw = dict(causal=spec.causal, softmax_scale=spec.softmax_scale, q_rope=d.get("q_rope"), k_rope=d.get("k_rope"),
-              q_scale=d.get("q_scale"), k_scale=d.get("k_scale"), cu_seqlens_q=d.get("cu_seqlens_q"),
-              cu_seqlens_k=d.get("cu_seqlens_k"), max_seqlen_q=max(lq), max_seqlen_k=max(lk), out=out, lse=lse,
-              schedule=args.schedule)
-    in_bytes = sum(t.numel() * t.element_size() for t in d.values() if isinstance(t, torch.Tensor))
     stream = torch.cuda.current_stream(dev)
     # Kernels per call: the attention kernel, plus the merge kernel when the
     # library splits the keys of each query tile (split-KV).
-    prm = pkg.make_params(d["q"], d["k"], d["v"], **kw)
-    ws = pkg.default_workspace(dev, pkg.workspace_bytes(prm))
-    prm.workspace, prm.workspace_bytes = ws.data_ptr(), ws.numel()
-    num_splits = pkg.plan(prm).num_splits
-    launches_per_step = 2 if num_splits > 1 else 1
+    inputs, d, kw, out, lse, num_splits, launches_per_step = prepare(spec, dev, args.schedule)
+    in_bytes = sum(t.numel() * t.element_size() for t in d.values() if isinstance(t, torch.Tensor))
 
     def step():
         pkg.forward(d["q"], d["k"], d["v"], stream=stream, **kw)
@@ -337,12 +440,7 @@ def main():
     time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize(dev)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    ev[0].record(stream)
-    for i in range(args.steps):
-        step()
-        ev[i + 1].record(stream)
-    torch.cuda.synchronize(dev)
+    per_launch, total_ms = time_calls(step, args.steps, stream)
     # The timed steps last milliseconds, nvidia-smi samples every 100 ms: keep
     # the same load running right after them until a second of samples exists.
     t_soak = time.perf_counter()
@@ -353,9 +451,7 @@ def main():
     barrier(world)
     clk = clocks.stop()
     pkg.check(device=dev)
-    per_launch = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
     median_ms = statistics.median(per_launch)
-    total_ms = ev[0].elapsed_time(ev[-1])
     total_ms = max_over_ranks(total_ms, world, dev)
     ms = total_ms / args.steps
     flops = spec.flops()
@@ -453,6 +549,12 @@ def main():
     if rank == 0 and world >= 1 and not args.no_cpu_baseline and args.gpus == 1:
         cpu = cpu_baseline(spec, inputs, args.cpu_seconds)
 
+    # The other workloads, after everything of the headline one (one GPU only).
+    others = None
+    if world == 1 and not args.no_workloads:
+        del d, inputs
+        others = time_other_workloads(args, dev, stream, peaks, peak_src)
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -471,7 +573,7 @@ def main():
             "pct_of_peak": 100.0 * value / world / peak,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak,
-                         "peak_source": f"bf16 burst{' x2 (fp8)' if spec.v_dtype == 'fp8' else ''}, {peak_src}",
+                         "peak_source": peak_label(spec, peak_src),
                          "traffic": profiled_traffic(args.workload)},
             "kernel_ms": kernel_ms,
             "median_ms": median_ms,
@@ -479,6 +581,7 @@ def main():
             "gpu_launches": args.steps * launches_per_step,
             "e2e": e2e,
             "cpu_baseline": cpu,
+            "workloads": others,
         }
         if spec.qk_dtype == "fp8":
             # against the nominal dense peaks as well (FP8 4.5 PF, BF16 2.25 PF)

@@ -203,10 +203,14 @@ attn_status attn_fwd(const attn_fwd_params *p, attn_stream_t stream);
  * must not allocate once it is running. It allocates nothing and calls no
  * allocating routine. The first call on a device looks up the array's device
  * address (cudaGetSymbolAddress, with that device current), so make it
- * before any stream capture. Every call clears and reuses the same array:
- * calls that overlap on the GPU (concurrent streams, or other threads) race
- * on it and must be serialised by the caller. Device-side wait timeouts of
- * this variant are not reported (there is no caller-visible error record).
+ * before any stream capture; calls outside a capture look it up again (no
+ * allocation), so the address stays valid across a cudaDeviceReset. Every
+ * call clears and reuses the same array: calls that overlap on the GPU
+ * (concurrent streams, or other threads) race on it and must be serialised
+ * by the caller. Device-side wait timeouts of this variant are not reported
+ * (there is no caller-visible error record): if a bounded wait inside the
+ * kernel ran out, which only a defect can cause, that call's O and LSE are
+ * undefined and nothing says so.
  * num_splits = 0 means "no split" here; an explicit split count needs more
  * scratch than the array holds. Returns UNSUPPORTED if a call would need more
  * scratch than the array holds, otherwise as attn_fwd. */
