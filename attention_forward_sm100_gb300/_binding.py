@@ -19,6 +19,7 @@ ATTN_OK = 0
 STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "cuda error", 4: "device timeout"}
 BACKENDS = {"tcgen05": 0, "simple": 1}
 SCHEDULES = {"dynamic": 0, "static": 1, "grid": 2}
+PAIR_CTA = {"auto": 0, "off": 1, "on": 2}
 DTYPES = {torch.bfloat16: 0, torch.float8_e4m3fn: 1}
 WORKSPACE_BYTES = 256
 
@@ -49,6 +50,7 @@ class Params(ctypes.Structure):
         ("fault_injection", ctypes.c_int32),
         ("num_splits", ctypes.c_int32),
         ("schedule", ctypes.c_int32),
+        ("pair_cta", ctypes.c_int32),
     ]
 
 
@@ -56,7 +58,7 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [("backend", ctypes.c_int32), ("rows_per_tile", ctypes.c_int32), ("work_tiles", ctypes.c_int64),
                 ("grid", ctypes.c_int32), ("block", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
                 ("k_stages", ctypes.c_int32), ("v_stages", ctypes.c_int32), ("tmem_columns", ctypes.c_int32),
-                ("num_splits", ctypes.c_int32)]
+                ("num_splits", ctypes.c_int32), ("pair_cta", ctypes.c_int32)]
 
 
 class WorkTile(ctypes.Structure):
@@ -198,7 +200,7 @@ def _check_layout(q, k, v, packed, out=None, lse=None, q_rope=None, k_rope=None,
 
 def make_params(q, k, v, *, causal, softmax_scale=None, q_rope=None, k_rope=None, q_scale=None, k_scale=None,
                 cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, out=None, lse=None,
-                workspace=None, backend="tcgen05", num_splits=0, schedule="dynamic") -> Params:
+                workspace=None, backend="tcgen05", num_splits=0, schedule="dynamic", pair_cta="auto") -> Params:
     """attn_fwd_params for torch tensors (shapes are read, nothing is allocated)."""
     packed = cu_seqlens_q is not None
     _check_layout(q, k, v, packed, out=out, lse=lse, q_rope=q_rope, k_rope=k_rope, q_scale=q_scale,
@@ -230,6 +232,7 @@ def make_params(q, k, v, *, causal, softmax_scale=None, q_rope=None, k_rope=None
     p.backend = BACKENDS[backend]
     p.num_splits = int(num_splits)
     p.schedule = SCHEDULES[schedule]
+    p.pair_cta = PAIR_CTA[pair_cta]
     p.q, p.k, p.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
     p.q_rope, p.k_rope = _ptr(q_rope), _ptr(k_rope)
     p.q_scale, p.k_scale = _ptr(q_scale), _ptr(k_scale)
@@ -261,7 +264,8 @@ def make_params(q, k, v, *, causal, softmax_scale=None, q_rope=None, k_rope=None
 
 def forward(q, k, v, *, causal=False, softmax_scale=None, q_rope=None, k_rope=None, q_scale=None, k_scale=None,
             cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, out=None, lse=None,
-            return_lse=True, workspace=None, backend="tcgen05", stream=None, num_splits=0, schedule="dynamic"):
+            return_lse=True, workspace=None, backend="tcgen05", stream=None, num_splits=0, schedule="dynamic",
+            pair_cta="auto"):
     """Fused attention forward on the GPU; returns (O, LSE).
 
     Fixed length: q [B,Sq,Hq,D], k [B,Sk,Hkv,D], v [B,Sk,Hkv,Dv] (e4m3 v:
@@ -273,8 +277,10 @@ def forward(q, k, v, *, causal=False, softmax_scale=None, q_rope=None, k_rope=No
     k_scale [B,Hkv,Sk] / [Hkv,Tk]. ``num_splits``: split-KV key ranges per
     query tile (0 = the library's choice, 1 = off; unmasked fixed-length
     problems only). ``schedule``: "dynamic" (default), "static" or "grid",
-    how work tiles reach CTAs (results are identical). Asynchronous on
-    ``stream`` (default: the current torch stream).
+    how work tiles reach CTAs (results are identical). ``pair_cta``: "auto"
+    (the library's choice), "off", or "on": two CTAs of a cluster share every
+    MMA (bf16, Dqk = Dv = 128, rope 0 or 64). Asynchronous on ``stream``
+    (default: the current torch stream).
     """
     for name, t in (("q", q), ("k", k), ("v", v), ("q_rope", q_rope), ("k_rope", k_rope), ("q_scale", q_scale),
                     ("k_scale", k_scale), ("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
@@ -292,7 +298,8 @@ def forward(q, k, v, *, causal=False, softmax_scale=None, q_rope=None, k_rope=No
     p = make_params(q, k, v, causal=causal, softmax_scale=softmax_scale, q_rope=q_rope, k_rope=k_rope,
                     q_scale=q_scale, k_scale=k_scale, cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k,
                     max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k, out=out, lse=lse,
-                    workspace=workspace, backend=backend, num_splits=num_splits, schedule=schedule)
+                    workspace=workspace, backend=backend, num_splits=num_splits, schedule=schedule,
+                    pair_cta=pair_cta)
     if workspace is None:
         with torch.cuda.device(dev):
             need = workspace_bytes(p)

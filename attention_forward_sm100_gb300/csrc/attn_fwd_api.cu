@@ -46,6 +46,15 @@ attn_status validate(const attn_fwd_params* p) {
   if (p->schedule != ATTN_SCHEDULE_DYNAMIC && p->schedule != ATTN_SCHEDULE_STATIC &&
       p->schedule != ATTN_SCHEDULE_GRID)
     return fail(ATTN_ERR_INVALID_ARG, "unknown schedule %d", p->schedule);
+  if (p->pair_cta != ATTN_PAIR_AUTO && p->pair_cta != ATTN_PAIR_OFF && p->pair_cta != ATTN_PAIR_ON)
+    return fail(ATTN_ERR_INVALID_ARG, "unknown pair_cta %d", p->pair_cta);
+  if (p->pair_cta == ATTN_PAIR_ON) {
+    if (p->backend != ATTN_BACKEND_TCGEN05) return fail(ATTN_ERR_UNSUPPORTED, "CTA pairs run on the tcgen05 backend only");
+    if (p->qk_dtype != ATTN_DTYPE_BF16 || p->v_dtype != ATTN_DTYPE_BF16 || p->head_dim_qk != 128 ||
+        p->head_dim_v != 128 || (p->rope_depth != 0 && p->rope_depth != 64))
+      return fail(ATTN_ERR_UNSUPPORTED, "CTA pairs support bf16 Q/K/V with Dqk = Dv = 128 and rope 0 or 64");
+    if (p->fault_injection != 0) return fail(ATTN_ERR_UNSUPPORTED, "fault injection is not available with CTA pairs");
+  }
   if (p->num_splits < 0 || p->num_splits > af::kMaxSplits)
     return fail(ATTN_ERR_INVALID_ARG, "num_splits %d outside [0, %d]", p->num_splits, af::kMaxSplits);
   if (p->num_splits >= 2) {
@@ -143,12 +152,20 @@ attn_status validate(const attn_fwd_params* p) {
   return ATTN_OK;
 }
 
+// CTA pairs for this call (pair_cta after validation; the automatic choice
+// keeps one CTA per MMA tile).
+bool use_pair(const attn_fwd_params* p) { return p->pair_cta == ATTN_PAIR_ON; }
+
 int tc05_variant(const attn_fwd_params* p) {
   if (p->qk_dtype == ATTN_DTYPE_FP8_E4M3)
     return p->v_dtype == ATTN_DTYPE_FP8_E4M3 ? af::kVarFp8QkvD128 : af::kVarFp8D128;
   if (p->head_dim_qk == 64) return af::kVarD64;
+  if (use_pair(p)) return p->rope_depth ? af::kVarD128Rope64Pair : af::kVarD128Pair;
   return p->rope_depth ? af::kVarD128Rope64 : af::kVarD128;
 }
+
+// Query rows of one work tile.
+int32_t rows_for(const attn_fwd_params* p) { return use_pair(p) ? af::kRowsPerTilePair : af::kRowsPerTile; }
 
 int sm_count_cached() {
   static std::atomic<int> cache[64];
@@ -168,6 +185,30 @@ int sm_count_cached() {
   return v;
 }
 
+// Clusters of two CTAs resident at once for a pair variant (cached per
+// device; half the SMs when the query is not possible).
+int max_clusters_cached(int variant) {
+  static std::atomic<int> cache[64][2];
+  const int slot = variant == af::kVarD128Rope64Pair ? 1 : 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return sm_count_cached() / 2;
+  }
+  if (dev < 0 || dev >= 64) return sm_count_cached() / 2;
+  int v = cache[dev][slot].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  v = af::tc05_max_clusters(variant);
+  if (v <= 0) return sm_count_cached() / 2;
+  cache[dev][slot].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+// Persistent work units of the launch: CTAs, or clusters for CTA pairs.
+int persistent_units(const attn_fwd_params* p) {
+  return use_pair(p) ? max_clusters_cached(tc05_variant(p)) : sm_count_cached();
+}
+
 int32_t kv_chunk_for(const attn_fwd_params* p) {
   const int64_t row = (int64_t)(p->head_dim_qk * qk_elem_bytes(p)) + 2ll * p->rope_depth +
                       (p->v_dtype == ATTN_DTYPE_FP8_E4M3 ? 1ll : 2ll) * p->head_dim_v;
@@ -178,14 +219,14 @@ int32_t kv_chunk_for(const attn_fwd_params* p) {
 }
 
 int64_t work_tiles_bound(const attn_fwd_params* p) {
-  const int64_t T = af::tiles_for(p->seqlen_q, af::kRowsPerTile);
+  const int64_t T = af::tiles_for(p->seqlen_q, rows_for(p));
   return (int64_t)p->batch * p->num_heads_q * T;
 }
 
 // Key ranges per query tile for `p` (1 = no split-KV). Explicit counts are
 // capped at the number of key tiles (of the longest sequence when packed);
 // 0 asks for the scheduler's choice on unmasked problems (for packed
-// sequences from the upper bound of the query tiles, B * ceil(max_len / 256)).
+// sequences from the upper bound of the query tiles, B * ceil(max_len / rows)).
 int32_t resolve_splits(const attn_fwd_params* p) {
   if (p == nullptr || p->num_splits == 1 || p->num_splits < 0 || p->num_splits > af::kMaxSplits ||
       p->backend != ATTN_BACKEND_TCGEN05 || p->causal || p->batch <= 0 || p->seqlen_q <= 0 ||
@@ -193,17 +234,19 @@ int32_t resolve_splits(const attn_fwd_params* p) {
     return 1;
   const int32_t kv_tiles = af::tiles_for(p->seqlen_k, af::kBlockN);
   if (p->num_splits >= 2) return p->num_splits < kv_tiles ? p->num_splits : kv_tiles;
-  return af::choose_splits(work_tiles_bound(p), kv_tiles, sm_count_cached(), af::kMaxSplits);
+  return af::choose_splits(work_tiles_bound(p), kv_tiles, persistent_units(p), af::kMaxSplits);
 }
 
 size_t round256(size_t n) { return (n + 255) & ~(size_t)255; }
 
 // CTAs launched for `work` work tiles: one per SM for the persistent
-// schedules, one per work tile otherwise.
+// schedules, one per work tile otherwise; CTA pairs launch two CTAs per
+// cluster and one cluster per resident cluster slot (or per work tile).
 int64_t grid_for(const attn_fwd_params* p, int64_t work) {
-  if (p->schedule == ATTN_SCHEDULE_GRID) return work;
-  const int sms = sm_count_cached();
-  return work < sms ? work : sms;
+  const int64_t per_unit = use_pair(p) ? 2 : 1;
+  if (p->schedule == ATTN_SCHEDULE_GRID) return per_unit * work;
+  const int64_t units = persistent_units(p);
+  return per_unit * (work < units ? work : units);
 }
 
 // Split-KV partial results in the workspace, after the 256 bytes of counters:
@@ -238,10 +281,10 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 4-D map over (depth, head, token, batch); box {box_d, 1, 128, 1}, 128-byte swizzle.
+// 4-D map over (depth, head, token, batch); box {box_d, 1, box_rows, 1}, 128-byte swizzle.
 attn_status make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int es, int64_t depth,
                      int64_t heads, int64_t tokens, int64_t batches, int64_t sh, int64_t st, int64_t sb,
-                     int box_d) {
+                     int box_d, int box_rows = af::kBlockN) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
   if (heads <= 1) sh = st > 0 ? st : depth;   // a size-1 dimension: any legal stride
@@ -249,7 +292,7 @@ attn_status make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt,
   if (tokens < 1) tokens = 1;
   cuuint64_t dims[4] = {(cuuint64_t)depth, (cuuint64_t)heads, (cuuint64_t)tokens, (cuuint64_t)batches};
   cuuint64_t strides[3] = {(cuuint64_t)(sh * es), (cuuint64_t)(st * es), (cuuint64_t)(sb * es)};
-  cuuint32_t box[4] = {(cuuint32_t)box_d, 1u, (cuuint32_t)af::kBlockN, 1u};
+  cuuint32_t box[4] = {(cuuint32_t)box_d, 1u, (cuuint32_t)box_rows, 1u};
   cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   CUresult r = fn(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -293,6 +336,8 @@ attn_status launch_tc05(const attn_fwd_params* p, cudaStream_t stream) {
   const int box_qk = fp8 ? 128 : 64;
   const int64_t tq = packed ? p->total_q : p->seqlen_q, tk = packed ? p->total_k : p->seqlen_k;
   const int64_t nb = packed ? 1 : p->batch;
+  // A CTA pair loads half of each K tile per CTA: 64-row K boxes.
+  const int k_rows = use_pair(p) ? af::kBlockN / 2 : af::kBlockN;
   attn_status st;
   if ((st = make_map(&prm.tm_q, p->q, qk_t, es, p->head_dim_qk, p->num_heads_q, tq, nb, p->q_stride[2],
                      p->q_stride[1], p->q_stride[0], box_qk)) != ATTN_OK)
@@ -302,7 +347,7 @@ attn_status launch_tc05(const attn_fwd_params* p, cudaStream_t stream) {
   const void* v_base = p->v != nullptr ? p->v : p->q;
   const void* kr_base = p->k_rope != nullptr ? p->k_rope : p->q_rope;
   if ((st = make_map(&prm.tm_k, k_base, qk_t, es, p->head_dim_qk, p->num_heads_kv, tk, nb, p->k_stride[2],
-                     p->k_stride[1], p->k_stride[0], box_qk)) != ATTN_OK)
+                     p->k_stride[1], p->k_stride[0], box_qk, k_rows)) != ATTN_OK)
     return st;
   if (p->v_dtype == ATTN_DTYPE_FP8_E4M3) {
     if ((st = make_map_vt(&prm.tm_v, p, v_base)) != ATTN_OK) return st;
@@ -315,7 +360,7 @@ attn_status launch_tc05(const attn_fwd_params* p, cudaStream_t stream) {
                        tq, nb, p->q_rope_stride[2], p->q_rope_stride[1], p->q_rope_stride[0], 64)) != ATTN_OK)
       return st;
     if ((st = make_map(&prm.tm_kr, kr_base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->rope_depth, 1, tk, nb,
-                       p->k_rope_stride[1], p->k_rope_stride[1], p->k_rope_stride[0], 64)) != ATTN_OK)
+                       p->k_rope_stride[1], p->k_rope_stride[1], p->k_rope_stride[0], 64, k_rows)) != ATTN_OK)
       return st;
   }
   prm.q_scale = p->q_scale;
@@ -334,7 +379,8 @@ attn_status launch_tc05(const attn_fwd_params* p, cudaStream_t stream) {
   prm.heads_q = p->num_heads_q;
   prm.heads_kv = p->num_heads_kv;
   prm.group = p->num_heads_q / p->num_heads_kv;
-  prm.tiles_per_seq = af::tiles_for(p->seqlen_q, af::kRowsPerTile);
+  prm.rows_per_tile = rows_for(p);
+  prm.tiles_per_seq = af::tiles_for(p->seqlen_q, prm.rows_per_tile);
   prm.kv_chunk = kv_chunk_for(p);
   prm.total_work = packed ? 0 : work_tiles_bound(p);
   prm.packed = packed ? 1 : 0;
@@ -458,10 +504,12 @@ attn_status attn_fwd_plan(const attn_fwd_params* p, attn_fwd_plan_info* out) {
     out->grid = (int32_t)out->work_tiles;
     out->block = 128;
     out->num_splits = 1;
+    out->pair_cta = ATTN_PAIR_OFF;
     return ATTN_OK;
   }
   const af::Tc05Config c = af::tc05_config(tc05_variant(p));
-  out->rows_per_tile = af::kRowsPerTile;
+  out->rows_per_tile = rows_for(p);
+  out->pair_cta = use_pair(p) ? ATTN_PAIR_ON : ATTN_PAIR_OFF;
   out->num_splits = resolve_splits(p);
   out->work_tiles = work_tiles_bound(p) * out->num_splits;
   const int64_t grid = grid_for(p, out->work_tiles);
@@ -492,7 +540,7 @@ int64_t attn_fwd_schedule(const attn_fwd_params* p, const int32_t* host_cu_seqle
     ++n;
   };
   if (host_cu_seqlens_q == nullptr) {
-    const int32_t T = af::tiles_for(p->seqlen_q, af::kRowsPerTile);
+    const int32_t T = af::tiles_for(p->seqlen_q, rows_for(p));
     const int32_t splits = resolve_splits(p);
     const int64_t total = (int64_t)p->batch * p->num_heads_q * T * splits;
     for (int64_t w = 0; w < total; ++w) emit(af::decode_fixed(w, T, splits, p->num_heads_q, group, chunk));
@@ -501,7 +549,7 @@ int64_t attn_fwd_schedule(const attn_fwd_params* p, const int32_t* host_cu_seqle
   const int32_t splits = resolve_splits(p);
   for (int b = 0; b < p->batch; ++b) {
     const int32_t len = host_cu_seqlens_q[b + 1] - host_cu_seqlens_q[b];
-    const int32_t T = af::tiles_for(len, af::kRowsPerTile);
+    const int32_t T = af::tiles_for(len, rows_for(p));
     for (int64_t wl = 0; wl < (int64_t)T * splits * p->num_heads_q; ++wl) {
       af::WorkTile w = af::decode_in_sequence(wl, b, T * splits, group, p->num_heads_kv, chunk);
       w.split = w.t % splits;

@@ -36,9 +36,21 @@
 //     (handed over through shared memory, the correction region of the
 //     layout page), rounds once to bf16 and stores it, or stores the fp32
 //     partial row of a split-KV range.
+//   * CTA pairs (the pair_cta option of the layout page's barrier set;
+//     Tc05Traits<..., PAIR = true>): two CTAs of a cluster on neighbouring
+//     SMs share every MMA. A work tile is then 512 rows; each of its two MMA
+//     tiles is 256 rows, 128 in each CTA, issued as one M = 256
+//     tcgen05.mma.cta_group::2 by the first CTA's issuers. Each CTA loads its
+//     own Q rows, half of each K tile (64 keys) and half of each V tile (64
+//     depth columns); all copies complete on the first CTA's barriers, the
+//     MMA commits arrive in both CTAs (multicast), and the softmax and
+//     epilogue warps of the second CTA report to the first CTA's barriers
+//     through the cluster window. Work indices are fetched by the first CTA
+//     and forwarded to the second through its shared memory.
 // Every wait is bounded: on timeout the CTA records an error in the
-// workspace, raises a shared abort flag that all waits poll, drains its
-// outstanding copies and MMAs, frees tensor memory and exits.
+// workspace, raises a shared abort flag that all waits poll (and, in a pair,
+// the peer's flag), drains its outstanding copies and MMAs, frees tensor
+// memory and exits.
 #pragma once
 #include <cuda_bf16.h>
 #include <math.h>
@@ -71,7 +83,9 @@ enum BarId : int {
   BAR_DRAIN = 23,        // final commit of the MMA threads
   BAR_ORDER = 24,        // +i, issue turn of MMA issuer i (forced ordering of the two Q tiles)
   BAR_Q_EMPTY1 = 26,     // last S MMA of Q tile 1 done
-  BAR_FIXED = 27         // then K_FULL[NK], K_EMPTY[NK], V_FULL[NV], V_EMPTY[NV]
+  BAR_WORK_FULL = 27,    // +slot, CTA pairs: work index written into the second CTA by the first
+  BAR_WORK_EMPTY = 29,   // +slot, CTA pairs: the second CTA read that work index
+  BAR_FIXED = 31         // then K_FULL[NK], K_EMPTY[NK], V_FULL[NV], V_EMPTY[NV]
 };
 
 constexpr int kSlotBytes = 48;   // shared-memory bytes of one SchedSlot entry
@@ -80,7 +94,7 @@ constexpr int kSlotBytes = 48;   // shared-memory bytes of one SchedSlot entry
 // correction warpgroup and the V producer lane.
 constexpr uint32_t kSchedConsumers = 2 + 128 + 128 + 128 + 1;
 
-template <int DQK_, int DR_, int DV_, bool FP8_, bool V8_ = false>
+template <int DQK_, int DR_, int DV_, bool FP8_, bool V8_ = false, bool PAIR_ = false>
 struct Tc05Traits {
   static constexpr int DQK = DQK_, DR = DR_, DV = DV_;
   static constexpr bool FP8 = FP8_;
@@ -88,17 +102,30 @@ struct Tc05Traits {
   // (K-major B operand of P.V) and P is rounded to e4m3 for kind::f8f6f4.
   static constexpr bool V8 = V8_;
   static_assert(!V8 || (FP8 && DV == 128), "e4m3 V needs e4m3 Q/K and Dv = 128");
+  // CTA pair: M = 256 MMAs over two CTAs; this CTA holds 128 of the rows,
+  // 64 keys of each K tile and 64 depth columns of each V tile.
+  static constexpr bool PAIR = PAIR_;
+  static_assert(!PAIR || (!FP8 && DQK == 128 && DV == 128), "CTA pairs: bf16 with Dqk = Dv = 128");
   static constexpr int BM = kBlockM, BN = kBlockN, NQ = 2;
+  static constexpr int MMA_M = PAIR ? 2 * kBlockM : kBlockM;   // rows of one MMA tile (both CTAs)
+  static constexpr int ROWS_PER_WORK = NQ * MMA_M;              // rows of one work tile
   static constexpr int QK_CHUNK_ELEMS = FP8 ? 128 : 64;   // elements of one 128-byte swizzle row
   static constexpr int QK_CHUNKS = DQK / QK_CHUNK_ELEMS;
   static constexpr int R_CHUNKS = DR / 64;
-  static constexpr int V_CHUNKS = V8 ? 1 : DV / 64;   // TMA boxes per V stage
+  static constexpr int V_CHUNKS = V8 ? 1 : (PAIR ? 1 : DV / 64);   // TMA boxes per V stage (this CTA)
   static constexpr int CHUNK_BYTES = 128 * 128;           // 128 rows x 128 bytes
+  static constexpr int K_ROWS = PAIR ? kBlockN / 2 : kBlockN;   // keys of a K stage held by this CTA
+  static constexpr int K_CHUNK_BYTES = K_ROWS * 128;
   static constexpr int Q_TILE_BYTES = (QK_CHUNKS + R_CHUNKS) * CHUNK_BYTES;
-  static constexpr int K_STAGE_BYTES = (QK_CHUNKS + R_CHUNKS) * CHUNK_BYTES;
+  static constexpr int K_STAGE_BYTES = (QK_CHUNKS + R_CHUNKS) * K_CHUNK_BYTES;
   static constexpr int V_STAGE_BYTES = V8 ? DV * 128 : V_CHUNKS * CHUNK_BYTES;
-  static constexpr int NK = DR > 0 ? 2 : (FP8 ? 4 : (DQK == 64 ? 4 : 3));
-  static constexpr int NV = DR > 0 ? 1 : (V8 ? 4 : (FP8 ? 3 : (DQK == 64 ? 4 : 2)));
+  static constexpr int NK = PAIR ? (DR > 0 ? 3 : 5) : (DR > 0 ? 2 : (FP8 ? 4 : (DQK == 64 ? 4 : 3)));
+  static constexpr int NV = PAIR ? (DR > 0 ? 3 : 4) : (DR > 0 ? 1 : (V8 ? 4 : (FP8 ? 3 : (DQK == 64 ? 4 : 2))));
+  // Bytes one phase of a Q / K / V full barrier waits for (a pair's first CTA
+  // counts both CTAs' copies).
+  static constexpr uint32_t Q_TX = (PAIR ? 2 : 1) * Q_TILE_BYTES;
+  static constexpr uint32_t K_TX = (PAIR ? 2 : 1) * K_STAGE_BYTES;
+  static constexpr uint32_t V_TX = (PAIR ? 2 : 1) * V_STAGE_BYTES;
 
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = NQ * Q_TILE_BYTES;
@@ -107,7 +134,8 @@ struct Tc05Traits {
   static constexpr int OFF_KS = OFF_RCPL + NQ * BM * 4;             // float [NQ][2][BN] (fp8)
   static constexpr int KS_BYTES = FP8 ? NQ * 2 * BN * 4 : 0;
   static constexpr int OFF_SCHED = OFF_KS + KS_BYTES;               // 2 slots x kSlotBytes
-  static constexpr int OFF_BAR = OFF_SCHED + 2 * kSlotBytes;
+  static constexpr int OFF_WORK = OFF_SCHED + 2 * kSlotBytes;       // CTA pairs: 2 x int64 work index
+  static constexpr int OFF_BAR = OFF_WORK + 16;
   static constexpr int NUM_BARS = BAR_FIXED + 2 * NK + 2 * NV;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
@@ -127,9 +155,9 @@ struct Tc05Traits {
   __host__ __device__ static constexpr uint32_t tm_o(int i) { return i ? 384u : 256u; }
 
   static constexpr uint32_t IDESC_S =
-      FP8 ? ptx::idesc_f32acc(0, 0, false, false, 128, 128) : ptx::idesc_f32acc(1, 1, false, false, 128, 128);
+      FP8 ? ptx::idesc_f32acc(0, 0, false, false, 128, 128) : ptx::idesc_f32acc(1, 1, false, false, MMA_M, 128);
   static constexpr uint32_t IDESC_PV =
-      V8 ? ptx::idesc_f32acc(0, 0, false, false, 128, DV) : ptx::idesc_f32acc(1, 1, false, true, 128, DV);
+      V8 ? ptx::idesc_f32acc(0, 0, false, false, 128, DV) : ptx::idesc_f32acc(1, 1, false, true, MMA_M, DV);
   // P.V instructions per half tile of 64 keys (K = 16 per bf16 instruction, 32 per e4m3).
   static constexpr int PV_INSTR_HALF = V8 ? 2 : 4;
   // TMEM columns of one half of P (64 keys as bf16 pairs or e4m3 quads).
@@ -163,7 +191,11 @@ struct Ctx {
   uint32_t* ws;
   uint64_t timeout_ns;
   int bar_off;
+  uint32_t rank;         // CTA pairs: this CTA's rank in the cluster (0 issues the MMAs); else 0
+  uint32_t peer_abort;   // CTA pairs: cluster-window address of the peer's abort flag; else 0
   __device__ __forceinline__ uint32_t bar(int i) const { return sbase + bar_off + 8u * (uint32_t)i; }
+  // Cluster-window address of barrier i in the pair's first CTA.
+  __device__ __forceinline__ uint32_t bar_lead(int i) const { return ptx::mapa(bar(i), 0); }
   __device__ __forceinline__ static int q_empty_id(int i) { return i == 0 ? BAR_Q_EMPTY : BAR_Q_EMPTY1; }
 };
 
@@ -171,15 +203,21 @@ __device__ __forceinline__ void raise_error(const Ctx& c, int role, int id) {
   if (atomicCAS(&c.ws[kWsErrorCode], 0u, (uint32_t)kDevErrTimeout) == 0u)
     atomicExch(&c.ws[kWsErrorInfo], ((uint32_t)blockIdx.x << 16) | ((uint32_t)role << 8) | (uint32_t)id);
   *c.abort_flag = 1;
+  if (c.peer_abort != 0u) ptx::st_cluster_u32(c.peer_abort, 1u);
 }
 
-// Warp-uniform bounded wait: every lane polls, the result is the same in all lanes.
+// Warp-uniform bounded wait: every lane polls, the result is the same in all
+// lanes. CLUSTER: the phase completes through arrivals of the peer CTA of a
+// pair, whose writes it must see (cluster-scope acquire).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_warp(const Ctx& c, int id, uint32_t parity, int role) {
   const uint32_t bar = c.bar(id);
-  if (__all_sync(kFull, ptx::mbar_test_wait(bar, parity))) return true;
+  if (__all_sync(kFull, CLUSTER ? ptx::mbar_test_wait_cluster(bar, parity) : ptx::mbar_test_wait(bar, parity)))
+    return true;
   const uint64_t t0 = __shfl_sync(kFull, ptx::globaltimer(), 0);
   for (uint32_t it = 1;; ++it) {
-    if (__all_sync(kFull, ptx::mbar_try_wait(bar, parity))) return true;
+    if (__all_sync(kFull, CLUSTER ? ptx::mbar_test_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity)))
+      return true;
     if ((it & 63u) == 0u) {
       if (__any_sync(kFull, *c.abort_flag != 0)) return false;
       const uint64_t now = __shfl_sync(kFull, ptx::globaltimer(), 0);
@@ -196,12 +234,14 @@ __device__ __forceinline__ bool wait_warp(const Ctx& c, int id, uint32_t parity,
 // suspending: a thread suspended in mbarrier.try_wait was seen to resume
 // hundreds of cycles after the phase completed, and every cycle an issuer
 // loses leaves the tensor core idle.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_one(const Ctx& c, int id, uint32_t parity, int role) {
   const uint32_t bar = c.bar(id);
-  if (ptx::mbar_test_wait(bar, parity)) return true;
+  auto test = [&]() { return CLUSTER ? ptx::mbar_test_wait_cluster(bar, parity) : ptx::mbar_test_wait(bar, parity); };
+  if (test()) return true;
   const uint64_t t0 = ptx::globaltimer();
   for (uint32_t it = 1;; ++it) {
-    if (ptx::mbar_test_wait(bar, parity)) return true;
+    if (test()) return true;
     if ((it & 255u) == 0u) {
       if (*c.abort_flag != 0) return false;
       if (ptx::globaltimer() - t0 > c.timeout_ns) {
@@ -235,17 +275,19 @@ struct Ring {
 };
 
 struct Geo {
-  int q0;      // first row (within its sequence) of Q tile 0
-  int n[2];    // K/V tiles each Q tile visits
+  int q0;       // first row (within its sequence) of the work tile
+  int row[2];   // first row of this CTA's 128 rows of MMA tile i
+  int n[2];     // K/V tiles MMA tile i visits
 };
 
-template <bool CAUSAL>
-__device__ __forceinline__ Geo tile_geo(const SchedSlot& s) {
+template <class T, bool CAUSAL>
+__device__ __forceinline__ Geo tile_geo(const SchedSlot& s, uint32_t rank) {
   Geo g;
-  g.q0 = s.t * kRowsPerTile;
+  g.q0 = s.t * T::ROWS_PER_WORK;
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    const int kv_end = CAUSAL ? min(s.lk, g.q0 + kBlockM * (i + 1)) : s.lk;
+    g.row[i] = g.q0 + T::MMA_M * i + kBlockM * (int)rank;
+    const int kv_end = CAUSAL ? min(s.lk, g.q0 + T::MMA_M * (i + 1)) : s.lk;
     g.n[i] = kv_end > 0 ? (kv_end + kBlockN - 1) / kBlockN : 0;
   }
   return g;
@@ -296,7 +338,7 @@ __device__ __forceinline__ SchedSlot decode_work(const Tc05Params& P, int64_t w,
       // one whose work index runs past the batch scans to its end).
       const int qs = P.cu_q[bb], qe = P.cu_q[bb + 1], ks = P.cu_k[bb], ke = P.cu_k[bb + 1];
       bad = qs < 0 || qe < qs || qe > P.total_q || ks < 0 || ke < ks || ke > P.total_k;
-      if (!bad) u = (int64_t)tiles_for(qe - qs, kRowsPerTile) * P.heads_q * P.num_splits;
+      if (!bad) u = (int64_t)tiles_for(qe - qs, P.rows_per_tile) * P.heads_q * P.num_splits;
     }
     const unsigned bad_lanes = __ballot_sync(kFull, bad);
     if (bad_lanes) {
@@ -318,7 +360,7 @@ __device__ __forceinline__ SchedSlot decode_work(const Tc05Params& P, int64_t w,
       cur.b += L;
       const int b = cur.b;
       const int qs = P.cu_q[b], qe = P.cu_q[b + 1], ks = P.cu_k[b], ke = P.cu_k[b + 1];
-      const WorkTile wt = decode_in_sequence(w - cur.base, b, tiles_for(qe - qs, kRowsPerTile) * P.num_splits,
+      const WorkTile wt = decode_in_sequence(w - cur.base, b, tiles_for(qe - qs, P.rows_per_tile) * P.num_splits,
                                              P.group, P.heads_kv, P.kv_chunk);
       s.valid = 1; s.b = b; s.h = wt.h; s.t = wt.t;
       s.q_start = qs; s.lq = qe - qs; s.k_start = ks; s.lk = ke - ks;
@@ -341,10 +383,30 @@ __device__ __forceinline__ SchedSlot decode_work(const Tc05Params& P, int64_t w,
 }
 
 // ---------------------------------------------------------------------------------------------
+// TMA load of one box into this CTA's shared memory, completing on barrier
+// `bar` (in a pair: on that barrier of the pair's first CTA).
+template <class T>
+__device__ __forceinline__ void load_box(const Ctx& c, uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
+                                         int c1, int c2, int c3) {
+  if constexpr (T::PAIR) ptx::tma_load_4d_pair(dst, map, ptx::mapa(bar, 0), c0, c1, c2, c3);
+  else ptx::tma_load_4d(dst, map, bar, c0, c1, c2, c3);
+}
+
+// Waits out this CTA's copies in flight after an abort. A pair's second CTA
+// cannot watch its copies (they complete on the first CTA's barriers): it
+// waits a fixed 200 us, far longer than any copy takes.
+__device__ __forceinline__ void pair_copy_grace() {
+  const uint64_t t0 = ptx::globaltimer();
+  while (ptx::globaltimer() - t0 < 200000ull) {
+  }
+}
+
 template <class T, bool CAUSAL>
 __device__ void role_load_qk(const Tc05Params& P, const Ctx& c) {
   const int lane = threadIdx.x & 31;
+  const bool lead = c.rank == 0;
   Ring<2> sched;
+  Ring<2> fwd;   // CTA pairs: work-index hand-over slots
   Ring<T::NK> kr;
   uint32_t q_empty_phase = 0;
   uint32_t k_fill_parity[T::NK];
@@ -354,7 +416,9 @@ __device__ void role_load_qk(const Tc05Params& P, const Ctx& c) {
 #pragma unroll
   for (int s = 0; s < T::NK; ++s) { k_fill_parity[s] = 0; k_used[s] = false; }
   Cursor cur;
-  int64_t w = blockIdx.x;
+  // The first work index is this CTA's own (a pair's: the cluster's).
+  int64_t w = T::PAIR ? (int64_t)ptx::cluster_id_x() : (int64_t)blockIdx.x;
+  const int64_t units = T::PAIR ? (int64_t)ptx::nclusters_x() : (int64_t)gridDim.x;
   bool aborted = false;
   while (true) {
     const SchedSlot s = decode_work(P, w, cur);
@@ -368,7 +432,7 @@ __device__ void role_load_qk(const Tc05Params& P, const Ctx& c) {
     __syncwarp();
     sched.next();
     if (!s.valid) break;
-    const Geo g = tile_geo<CAUSAL>(s);
+    const Geo g = tile_geo<T, CAUSAL>(s, c.rank);
     const int n1 = g.n[1];
     if (n1 > 0) {
       const int hk = s.h / P.group;
@@ -376,12 +440,12 @@ __device__ void role_load_qk(const Tc05Params& P, const Ctx& c) {
       auto load_q = [&](int i) {
         const uint32_t bar = c.bar(BAR_Q_FULL + i);
         const uint32_t dst = c.sbase + T::OFF_Q + i * T::Q_TILE_BYTES;
-        const int row = s.q_start + g.q0 + kBlockM * i;
-        ptx::mbar_expect_tx(bar, T::Q_TILE_BYTES);
+        const int row = s.q_start + g.row[i];
+        if (lead) ptx::mbar_expect_tx(bar, T::Q_TX);
 #pragma unroll
         for (int ch = 0; ch < T::QK_CHUNKS; ++ch)
-          ptx::tma_load_4d(dst + ch * T::CHUNK_BYTES, &P.tm_q, bar, ch * T::QK_CHUNK_ELEMS, s.h, row, qb);
-        if (T::DR > 0) ptx::tma_load_4d(dst + T::QK_CHUNKS * T::CHUNK_BYTES, &P.tm_qr, bar, 0, s.h, row, qb);
+          load_box<T>(c, dst + ch * T::CHUNK_BYTES, &P.tm_q, bar, ch * T::QK_CHUNK_ELEMS, s.h, row, qb);
+        if (T::DR > 0) load_box<T>(c, dst + T::QK_CHUNKS * T::CHUNK_BYTES, &P.tm_qr, bar, 0, s.h, row, qb);
       };
       // Q tile 0, K_0, then Q tile 1: each Q region is refilled as soon as
       // its own last S MMA of the previous work tile is done.
@@ -395,12 +459,13 @@ __device__ void role_load_qk(const Tc05Params& P, const Ctx& c) {
         if (lane == 0) {
           const uint32_t bar = c.bar(T::BAR_K_FULL + kr.idx);
           const uint32_t dst = c.sbase + T::OFF_K + kr.idx * T::K_STAGE_BYTES;
-          const int row = s.k_start + kBlockN * j;
-          ptx::mbar_expect_tx(bar, T::K_STAGE_BYTES);
+          // a pair's CTA r holds keys [64 r, 64 r + 64) of the tile
+          const int row = s.k_start + kBlockN * j + (T::PAIR ? T::K_ROWS * (int)c.rank : 0);
+          if (lead) ptx::mbar_expect_tx(bar, T::K_TX);
 #pragma unroll
           for (int ch = 0; ch < T::QK_CHUNKS; ++ch)
-            ptx::tma_load_4d(dst + ch * T::CHUNK_BYTES, &P.tm_k, bar, ch * T::QK_CHUNK_ELEMS, hk, row, qb);
-          if (T::DR > 0) ptx::tma_load_4d(dst + T::QK_CHUNKS * T::CHUNK_BYTES, &P.tm_kr, bar, 0, 0, row, qb);
+            load_box<T>(c, dst + ch * T::K_CHUNK_BYTES, &P.tm_k, bar, ch * T::QK_CHUNK_ELEMS, hk, row, qb);
+          if (T::DR > 0) load_box<T>(c, dst + T::QK_CHUNKS * T::K_CHUNK_BYTES, &P.tm_kr, bar, 0, 0, row, qb);
         }
         k_fill_parity[kr.idx] = kr.phase;
         k_used[kr.idx] = true;
@@ -415,25 +480,51 @@ __device__ void role_load_qk(const Tc05Params& P, const Ctx& c) {
       if (aborted) break;
     }
     // Next work index: from the shared counter (dynamic), one grid stride on
-    // (static), or none (one CTA per work tile).
+    // (static), or none (one CTA per work tile). A pair's first CTA takes it
+    // from the counter and writes it into the second CTA's shared memory.
     if (P.schedule == ATTN_SCHEDULE_DYNAMIC) {
-      int64_t nw = 0;
-      if (lane == 0) nw = (int64_t)gridDim.x + (int64_t)atomicAdd(&c.ws[kWsTileCounter], 1u);
-      w = __shfl_sync(kFull, nw, 0);
+      if (!T::PAIR || lead) {
+        int64_t nw = 0;
+        if (lane == 0) nw = units + (int64_t)atomicAdd(&c.ws[kWsTileCounter], 1u);
+        w = __shfl_sync(kFull, nw, 0);
+      }
+      if constexpr (T::PAIR) {
+        const uint32_t slot = c.sbase + T::OFF_WORK + 8u * fwd.idx;
+        if (lead) {
+          if (!wait_warp<true>(c, BAR_WORK_EMPTY + fwd.idx, fwd.phase ^ 1u, kRoleLoadQK)) { aborted = true; break; }
+          if (lane == 0) {
+            ptx::st_cluster_u32(ptx::mapa(slot, 1), (uint32_t)(uint64_t)w);
+            ptx::st_cluster_u32(ptx::mapa(slot + 4u, 1), (uint32_t)((uint64_t)w >> 32));
+            ptx::mbar_arrive_cluster(ptx::mapa(c.bar(BAR_WORK_FULL + fwd.idx), 1));
+          }
+        } else {
+          if (!wait_warp<true>(c, BAR_WORK_FULL + fwd.idx, fwd.phase, kRoleLoadQK)) { aborted = true; break; }
+          const volatile uint32_t* ws = reinterpret_cast<const volatile uint32_t*>(c.smem + T::OFF_WORK + 8 * fwd.idx);
+          w = (int64_t)(((uint64_t)ws[1] << 32) | (uint64_t)ws[0]);
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive_cluster(c.bar_lead(BAR_WORK_EMPTY + fwd.idx));
+        }
+        __syncwarp();
+        fwd.next();
+      }
     } else if (P.schedule == ATTN_SCHEDULE_STATIC) {
-      w += gridDim.x;
+      w += units;
     } else {
       w = INT64_MAX;
     }
   }
   if (aborted && lane == 0) {
-    // Let every copy this warp issued land before the CTA exits.
+    if (lead) {
+      // Let every copy this warp issued land before the CTA exits.
 #pragma unroll
-    for (int s = 0; s < T::NK; ++s)
-      if (k_used[s]) wait_drain(c, T::BAR_K_FULL + s, k_fill_parity[s]);
+      for (int s = 0; s < T::NK; ++s)
+        if (k_used[s]) wait_drain(c, T::BAR_K_FULL + s, k_fill_parity[s]);
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
-      if (q_loaded[i]) wait_drain(c, BAR_Q_FULL + i, q_fill_parity);
+      for (int i = 0; i < 2; ++i)
+        if (q_loaded[i]) wait_drain(c, BAR_Q_FULL + i, q_fill_parity);
+    } else {
+      pair_copy_grace();
+    }
   }
   __syncwarp();
 }
@@ -441,6 +532,7 @@ __device__ void role_load_qk(const Tc05Params& P, const Ctx& c) {
 template <class T, bool CAUSAL>
 __device__ void role_load_v(const Tc05Params& P, const Ctx& c) {
   const int lane = threadIdx.x & 31;
+  const bool lead = c.rank == 0;
   Ring<2> sched;
   Ring<T::NV> vr;
   uint32_t v_fill_parity[T::NV];
@@ -455,7 +547,7 @@ __device__ void role_load_v(const Tc05Params& P, const Ctx& c) {
     if (lane == 0) ptx::mbar_arrive(c.bar(BAR_SCHED_EMPTY + sched.idx));
     sched.next();
     if (!s.valid) break;
-    const Geo g = tile_geo<CAUSAL>(s);
+    const Geo g = tile_geo<T, CAUSAL>(s, c.rank);
     const int hk = s.h / P.group;
     const int vb = P.packed ? 0 : s.b;
     for (int j = 0; j < g.n[1]; ++j) {
@@ -468,11 +560,14 @@ __device__ void role_load_v(const Tc05Params& P, const Ctx& c) {
         const uint32_t bar = c.bar(T::BAR_V_FULL + vr.idx);
         const uint32_t dst = c.sbase + T::OFF_V + vr.idx * T::V_STAGE_BYTES;
         const int row = s.k_start + kBlockN * j;
-        ptx::mbar_expect_tx(bar, T::V_STAGE_BYTES);
+        if (lead) ptx::mbar_expect_tx(bar, T::V_TX);
         if (T::V8) {
           // depth-major e4m3 V: coordinates (key, depth row, head, batch); the
           // key coordinate is a multiple of 128 (fixed-length sequences only)
           ptx::tma_load_4d(dst, &P.tm_v, bar, row, 0, hk, vb);
+        } else if (T::PAIR) {
+          // a pair's CTA r holds depth columns [64 r, 64 r + 64) of the tile
+          load_box<T>(c, dst, &P.tm_v, bar, 64 * (int)c.rank, hk, row, vb);
         } else {
 #pragma unroll
           for (int ch = 0; ch < T::V_CHUNKS; ++ch)
@@ -486,9 +581,13 @@ __device__ void role_load_v(const Tc05Params& P, const Ctx& c) {
     if (aborted) break;
   }
   if (aborted && lane == 0) {
+    if (lead) {
 #pragma unroll
-    for (int s = 0; s < T::NV; ++s)
-      if (v_used[s]) wait_drain(c, T::BAR_V_FULL + s, v_fill_parity[s]);
+      for (int s = 0; s < T::NV; ++s)
+        if (v_used[s]) wait_drain(c, T::BAR_V_FULL + s, v_fill_parity[s]);
+    } else {
+      pair_copy_grace();
+    }
   }
   __syncwarp();
 }
@@ -506,12 +605,15 @@ __device__ __forceinline__ void issue_s(const Ctx& c, int i, uint32_t kstage) {
   for (int kk = B; kk < E; ++kk) {
     if (T::FP8) {
       ptx::mma_fp8_ss_lo<HI, HI, T::IDESC_S>(d, qa + kk * 2, ka + kk * 2, kk > 0);
-    } else if (kk < T::DQK / 16) {
-      const uint32_t off = ((kk >> 2) * T::CHUNK_BYTES + (kk & 3) * 32) >> 4;
-      ptx::mma_bf16_ss_lo<HI, HI, T::IDESC_S>(d, qa + off, ka + off, kk > 0);
     } else {
-      const uint32_t off = (T::QK_CHUNKS * T::CHUNK_BYTES + (kk - T::DQK / 16) * 32) >> 4;
-      ptx::mma_bf16_ss_lo<HI, HI, T::IDESC_S>(d, qa + off, ka + off, 1u);
+      // Q chunks are 128 rows, K chunks K_ROWS rows (64 in a pair)
+      const bool rope = kk >= T::DQK / 16;
+      const uint32_t qo = (rope ? (T::QK_CHUNKS * T::CHUNK_BYTES + (kk - T::DQK / 16) * 32)
+                                : ((kk >> 2) * T::CHUNK_BYTES + (kk & 3) * 32)) >> 4;
+      const uint32_t ko = (rope ? (T::QK_CHUNKS * T::K_CHUNK_BYTES + (kk - T::DQK / 16) * 32)
+                                : ((kk >> 2) * T::K_CHUNK_BYTES + (kk & 3) * 32)) >> 4;
+      if constexpr (T::PAIR) ptx::mma_bf16_ss_lo_pair<HI, HI, T::IDESC_S>(d, qa + qo, ka + ko, kk > 0);
+      else ptx::mma_bf16_ss_lo<HI, HI, T::IDESC_S>(d, qa + qo, ka + ko, kk > 0);
     }
   }
 }
@@ -533,8 +635,12 @@ __device__ __forceinline__ void issue_pv(const Ctx& c, int i, uint32_t vstage, b
     const uint32_t va =
         ptx::sdesc_lo(ptx::opaque(c.sbase + T::OFF_V + vstage * T::V_STAGE_BYTES), T::CHUNK_BYTES);
 #pragma unroll
-    for (int kk = 4 * HALF; kk < 4 * HALF + 4; ++kk)
-      ptx::mma_bf16_ts_lo<HI, T::IDESC_PV>(d, a + kk * 8, va + kk * (2048 >> 4), (accumulate || kk > 0) ? 1u : 0u);
+    for (int kk = 4 * HALF; kk < 4 * HALF + 4; ++kk) {
+      if constexpr (T::PAIR)
+        ptx::mma_bf16_ts_lo_pair<HI, T::IDESC_PV>(d, a + kk * 8, va + kk * (2048 >> 4), (accumulate || kk > 0) ? 1u : 0u);
+      else
+        ptx::mma_bf16_ts_lo<HI, T::IDESC_PV>(d, a + kk * 8, va + kk * (2048 >> 4), (accumulate || kk > 0) ? 1u : 0u);
+    }
   }
 }
 
@@ -547,9 +653,18 @@ __device__ __forceinline__ void issue_pv(const Ctx& c, int i, uint32_t vstage, b
 // as many K/V tiles as tile 1, pads with empty groups so that the
 // alternation never has to wait for the next work tile. K, V and Q stages are
 // released by one commit from each issuer.
+// Commit of the issuing thread's MMAs to barrier `id`: in a pair, to that
+// barrier in both CTAs (ALL) or in the first CTA only.
+template <class T, bool ALL = true>
+__device__ __forceinline__ void commit(const Ctx& c, int id) {
+  if constexpr (T::PAIR) ptx::mma_commit_pair(c.bar(id), ALL ? (uint16_t)3 : (uint16_t)1);
+  else ptx::mma_commit(c.bar(id));
+}
+
 template <class T, bool CAUSAL>
 __device__ void role_mma(const Tc05Params& P, const Ctx& c, const int i) {
-  // Runs on lane 0 of warp 12 + i only: one thread issues, waits and commits.
+  // Runs on lane 0 of warp 12 + i only (in a pair: of the first CTA): one
+  // thread issues, waits and commits.
   const int role = kRoleMma;
   Ring<2> sched;
   Ring<T::NK> kr;   // stage of the next K tile
@@ -563,17 +678,23 @@ __device__ void role_mma(const Tc05Params& P, const Ctx& c, const int i) {
     aborted = true;                        \
     break;                                 \
   }
+  // barriers that the peer CTA of a pair arrives on
+#define AF_WAIT_CL(id, par)                         \
+  if (!wait_one<T::PAIR>(c, (id), (par), role)) {   \
+    aborted = true;                                 \
+    break;                                          \
+  }
   while (true) {
     if (!wait_one(c, BAR_SCHED_FULL + sched.idx, sched.phase, role)) { aborted = true; break; }
     const SchedSlot s = read_slot(c, sched.idx, T::OFF_SCHED);
     ptx::mbar_arrive(c.bar(BAR_SCHED_EMPTY + sched.idx));
     sched.next();
     if (!s.valid) break;
-    const Geo g = tile_geo<CAUSAL>(s);
+    const Geo g = tile_geo<T, CAUSAL>(s, c.rank);
     const int n = g.n[i], n1 = g.n[1];
     if (n1 == 0) {
       // No keys: keep the per-tile O-free handshake in step with the epilogue.
-      AF_WAIT(BAR_O_FREE + i, ofree_phase ^ 1u);
+      AF_WAIT_CL(BAR_O_FREE + i, ofree_phase ^ 1u);
       ofree_phase ^= 1u;
       continue;
     }
@@ -588,7 +709,7 @@ __device__ void role_mma(const Tc05Params& P, const Ctx& c, const int i) {
       // the softmax warps keep tensor and shared memory busy).
       if (has_pv) {
         if (grp == 1) {
-          AF_WAIT(BAR_O_FREE + i, ofree_phase ^ 1u);
+          AF_WAIT_CL(BAR_O_FREE + i, ofree_phase ^ 1u);
           ofree_phase ^= 1u;
         }
         AF_WAIT(T::BAR_V_FULL + vr.idx, vr.phase);
@@ -596,16 +717,16 @@ __device__ void role_mma(const Tc05Params& P, const Ctx& c, const int i) {
       if (has_s) AF_WAIT(T::BAR_K_FULL + kr.idx, kr.phase);
       if (!wait_one(c, BAR_ORDER + i, order_phase ^ order_flip, role)) { aborted = true; break; }
       order_phase ^= 1u;
-      if (has_pv) AF_WAIT(BAR_P_LO + i, p_phase);
+      if (has_pv) AF_WAIT_CL(BAR_P_LO + i, p_phase);
       ptx::tc_fence_after();
       if (has_pv) {
         issue_pv<T, 0>(c, i, vr.idx, grp > 1);
-        AF_WAIT(BAR_P_HI + i, p_phase);
+        AF_WAIT_CL(BAR_P_HI + i, p_phase);
         p_phase ^= 1u;
         ptx::tc_fence_after();
         issue_pv<T, 1>(c, i, vr.idx, true);
-        ptx::mma_commit(c.bar(T::BAR_V_EMPTY + vr.idx));
-        if (grp == n) ptx::mma_commit(c.bar(BAR_O_FINAL + i));
+        commit<T>(c, T::BAR_V_EMPTY + vr.idx);
+        if (grp == n) commit<T>(c, BAR_O_FINAL + i);
         vr.next();
       }
       if (has_s) {
@@ -614,9 +735,9 @@ __device__ void role_mma(const Tc05Params& P, const Ctx& c, const int i) {
         issue_s<T, 0, T::S_INSTR - T::S_AFTER_HANDOFF>(c, i, kr.idx);
         ptx::mbar_arrive(c.bar(BAR_ORDER + (i ^ 1)));
         issue_s<T, T::S_INSTR - T::S_AFTER_HANDOFF, T::S_INSTR>(c, i, kr.idx);
-        ptx::mma_commit(c.bar(BAR_S_FULL + i));
-        ptx::mma_commit(c.bar(T::BAR_K_EMPTY + kr.idx));
-        if (grp == n - 1) ptx::mma_commit(c.bar(Ctx::q_empty_id(i)));
+        commit<T>(c, BAR_S_FULL + i);
+        commit<T>(c, T::BAR_K_EMPTY + kr.idx);
+        if (grp == n - 1) commit<T>(c, Ctx::q_empty_id(i));
         kr.next();
       } else {
         ptx::mbar_arrive(c.bar(BAR_ORDER + (i ^ 1)));   // the other issuer's turn
@@ -624,19 +745,20 @@ __device__ void role_mma(const Tc05Params& P, const Ctx& c, const int i) {
       if (!has_pv && !has_s) {
         // A K/V tile only the other Q tile visits: release this issuer's share.
         AF_WAIT(T::BAR_K_FULL + kr.idx, kr.phase);
-        ptx::mma_commit(c.bar(T::BAR_K_EMPTY + kr.idx));
+        commit<T>(c, T::BAR_K_EMPTY + kr.idx);
         kr.next();
         AF_WAIT(T::BAR_V_FULL + vr.idx, vr.phase);
-        ptx::mma_commit(c.bar(T::BAR_V_EMPTY + vr.idx));
+        commit<T>(c, T::BAR_V_EMPTY + vr.idx);
         vr.next();
       }
     }
     if (aborted) break;
   }
 #undef AF_WAIT
+#undef AF_WAIT_CL
   // Drain: the arrive of this commit follows every MMA and commit this thread
   // issued (both issuers commit; the phase completes after both).
-  ptx::mma_commit(c.bar(BAR_DRAIN));
+  commit<T, false>(c, BAR_DRAIN);
   wait_drain(c, BAR_DRAIN, 0);
   (void)aborted;
 }
@@ -659,12 +781,12 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
     ptx::mbar_arrive(c.bar(BAR_SCHED_EMPTY + sched.idx));
     sched.next();
     if (!s.valid) return;
-    const Geo g = tile_geo<CAUSAL>(s);
+    const Geo g = tile_geo<T, CAUSAL>(s, c.rank);
     const int n = g.n[i];
-    const int qi = g.q0 + kBlockM * i + tid;     // row within the sequence
+    const int qi = g.row[i] + tid;               // row within the sequence
     const bool row_valid = qi < s.lq;
     const int lim = CAUSAL ? min(s.lk, qi + 1) : s.lk;   // keys visible to this row
-    const int first_row = g.q0 + kBlockM * i;
+    const int first_row = g.row[i];
     // LSE element: [B][Hq][Sq] (or [Hq][Tq] packed); a split-KV range writes
     // its partial LSE to copy `split` of that layout, [split][B][Hq][Sq] (or
     // [split][Hq][Tq]).
@@ -792,7 +914,13 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(c.bar((half == 0 ? BAR_P_LO : BAR_P_HI) + i));
+        if constexpr (T::PAIR) {
+          // one arrival per warp on the first CTA's barrier
+          __syncwarp();
+          if ((threadIdx.x & 31) == 0) ptx::mbar_arrive_cluster(c.bar_lead((half == 0 ? BAR_P_LO : BAR_P_HI) + i));
+        } else {
+          ptx::mbar_arrive(c.bar((half == 0 ? BAR_P_LO : BAR_P_HI) + i));
+        }
       }
       float s0, s1, s2, s3;
       ptx::f2_unpack(acc0, s0, s1);
@@ -856,7 +984,7 @@ __device__ void role_correction(const Tc05Params& P, const Ctx& c) {
     ptx::mbar_arrive(c.bar(BAR_SCHED_EMPTY + sched.idx));
     sched.next();
     if (!s.valid) return;
-    const Geo g = tile_geo<CAUSAL>(s);
+    const Geo g = tile_geo<T, CAUSAL>(s, c.rank);
 #pragma unroll 1
     for (int i = 0; i < 2; ++i) {
       // Epilogue of Q tile i: O = O / l, rounded once to bf16, stored row by row.
@@ -864,7 +992,7 @@ __device__ void role_correction(const Tc05Params& P, const Ctx& c) {
       stats_phase[i] ^= 1u;
       const float rl = rcpl_sm[i * kBlockM + tid];
       ptx::mbar_arrive(c.bar(BAR_STATS_FREE + i));
-      const int qi = g.q0 + kBlockM * i + tid;
+      const int qi = g.row[i] + tid;
       const bool row_valid = qi < s.lq;
       uint16_t* orow = P.o + (int64_t)s.b * P.o_stride_b + (int64_t)(s.q_start + qi) * P.o_stride_t +
                        (int64_t)s.h * P.o_stride_h;
@@ -904,7 +1032,13 @@ __device__ void role_correction(const Tc05Params& P, const Ctx& c) {
         for (int e = 0; e < T::DV / 8; ++e) d[e] = make_uint4(0u, 0u, 0u, 0u);
       }
       ptx::tc_fence_before();
-      ptx::mbar_arrive(c.bar(BAR_O_FREE + i));
+      if constexpr (T::PAIR) {
+        // one arrival per warp on the first CTA's barrier (its MMAs write both CTAs' O)
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) ptx::mbar_arrive_cluster(c.bar_lead(BAR_O_FREE + i));
+      } else {
+        ptx::mbar_arrive(c.bar(BAR_O_FREE + i));
+      }
     }
   }
 }
@@ -929,26 +1063,33 @@ __global__ void __launch_bounds__(512, 1) fa_tc05_kernel(const __grid_constant__
   c.abort_flag = reinterpret_cast<volatile int*>(smem + T::OFF_ABORT);
   c.bar_off = T::OFF_BAR;
   c.timeout_ns = P.timeout_ns;
-  if (c.sbase & 1023u) {  // the swizzled tiles need a 1024-byte aligned base
+  c.rank = T::PAIR ? ptx::cluster_ctarank() : 0u;
+  c.peer_abort = 0u;
+  if (c.sbase & 1023u) {  // the swizzled tiles need a 1024-byte aligned base (same in both CTAs of a pair)
     if (threadIdx.x == 0) atomicCAS(&P.ws[kWsErrorCode], 0u, 2u);
     return;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Barriers that the second CTA of a pair reports to per warp (4 warps per CTA).
+  const uint32_t warp_count = T::PAIR ? 8u : 128u;
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(c.bar(BAR_Q_FULL + i), 1);
       ptx::mbar_init(c.bar(BAR_S_FULL + i), 1);
-      ptx::mbar_init(c.bar(BAR_P_LO + i), 128);
+      ptx::mbar_init(c.bar(BAR_P_LO + i), warp_count);
       ptx::mbar_init(c.bar(BAR_STATS + i), 128);
-      ptx::mbar_init(c.bar(BAR_P_HI + i), 128);
+      ptx::mbar_init(c.bar(BAR_P_HI + i), warp_count);
       ptx::mbar_init(c.bar(BAR_ORDER + i), 1);
       ptx::mbar_init(c.bar(BAR_O_FINAL + i), 1);
-      ptx::mbar_init(c.bar(BAR_O_FREE + i), 128);
+      ptx::mbar_init(c.bar(BAR_O_FREE + i), warp_count);
       ptx::mbar_init(c.bar(BAR_STATS_FREE + i), 128);
       ptx::mbar_init(c.bar(BAR_KS + i), 128);
       ptx::mbar_init(c.bar(BAR_SCHED_FULL + i), 1);
-      ptx::mbar_init(c.bar(BAR_SCHED_EMPTY + i), kSchedConsumers);
+      // a pair's second CTA runs no MMA issuers
+      ptx::mbar_init(c.bar(BAR_SCHED_EMPTY + i), kSchedConsumers - (c.rank != 0 ? 2u : 0u));
+      ptx::mbar_init(c.bar(BAR_WORK_FULL + i), 1);
+      ptx::mbar_init(c.bar(BAR_WORK_EMPTY + i), 1);
     }
     ptx::mbar_init(c.bar(BAR_Q_EMPTY), 1);
     ptx::mbar_init(c.bar(BAR_Q_EMPTY1), 1);
@@ -967,8 +1108,13 @@ __global__ void __launch_bounds__(512, 1) fa_tc05_kernel(const __grid_constant__
     ptx::fence_mbar_init();
   }
   if (warp == 12) {
-    ptx::tmem_alloc(c.sbase + T::OFF_TMEM_SLOT, T::TMEM_COLS);
-    ptx::tmem_relinquish();
+    if constexpr (T::PAIR) {
+      ptx::tmem_alloc_pair(c.sbase + T::OFF_TMEM_SLOT, T::TMEM_COLS);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(c.sbase + T::OFF_TMEM_SLOT, T::TMEM_COLS);
+      ptx::tmem_relinquish();
+    }
   }
   if (warp == 14 && lane == 0) {
     ptx::prefetch_tmap(&P.tm_q);
@@ -980,9 +1126,14 @@ __global__ void __launch_bounds__(512, 1) fa_tc05_kernel(const __grid_constant__
     }
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  // A pair's barriers must be initialised in both CTAs before either CTA
+  // copies into, or arrives on, the other's.
+  __syncwarp();
+  if constexpr (T::PAIR) ptx::cluster_sync();
+  else __syncthreads();
   ptx::tc_fence_after();
   c.tmem = *reinterpret_cast<volatile uint32_t*>(smem + T::OFF_TMEM_SLOT);
+  if constexpr (T::PAIR) c.peer_abort = ptx::mapa(c.sbase + T::OFF_ABORT, c.rank ^ 1u);
 
   const int wg = warp >> 2;
   if (wg < 2) {
@@ -994,7 +1145,7 @@ __global__ void __launch_bounds__(512, 1) fa_tc05_kernel(const __grid_constant__
   } else {
     setmaxnreg_dec<T::REG_MISC>();
     if (warp == 12 || warp == 13) {
-      if (lane == 0) role_mma<T, CAUSAL>(P, c, warp - 12);
+      if (lane == 0 && c.rank == 0) role_mma<T, CAUSAL>(P, c, warp - 12);
       __syncwarp();
     }
     else if (warp == 14) role_load_qk<T, CAUSAL>(P, c);
@@ -1002,10 +1153,15 @@ __global__ void __launch_bounds__(512, 1) fa_tc05_kernel(const __grid_constant__
   }
 
   ptx::tc_fence_before();
-  __syncthreads();
+  // Both CTAs of a pair are done with the MMAs (which use both CTAs' tensor
+  // and shared memory) before either frees its tensor memory or exits.
+  __syncwarp();
+  if constexpr (T::PAIR) ptx::cluster_sync();
+  else __syncthreads();
   if (warp == 12) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(c.tmem, T::TMEM_COLS);
+    if constexpr (T::PAIR) ptx::tmem_dealloc_pair(c.tmem, T::TMEM_COLS);
+    else ptx::tmem_dealloc(c.tmem, T::TMEM_COLS);
   }
   if (threadIdx.x == 0) {
     __threadfence();
@@ -1017,13 +1173,61 @@ __global__ void __launch_bounds__(512, 1) fa_tc05_kernel(const __grid_constant__
   }
 }
 
+// Launch configuration of a pair variant: clusters of two CTAs.
+template <class T>
+cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(512, 1, 1);
+  cfg.dynamicSmemBytes = T::SMEM_BYTES;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
 template <class T>
 cudaError_t tc05_launch_t(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream) {
   auto kern = causal ? fa_tc05_kernel<T, true> : fa_tc05_kernel<T, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  kern<<<grid, 512, T::SMEM_BYTES, stream>>>(prm);
+  if constexpr (T::PAIR) {
+    if (grid % 2 != 0) return cudaErrorInvalidValue;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = pair_config<T>(grid, stream, attr);
+    e = cudaLaunchKernelEx(&cfg, kern, prm);
+    if (e != cudaSuccess) return e;
+  } else {
+    kern<<<grid, 512, T::SMEM_BYTES, stream>>>(prm);
+  }
   return cudaGetLastError();
+}
+
+// Clusters of a pair variant that can be resident at once on the current
+// device (0 if the query fails or the variant is not a pair variant).
+template <class T>
+int tc05_max_clusters_t() {
+  if constexpr (!T::PAIR) {
+    return 0;
+  } else {
+    auto kern = fa_tc05_kernel<T, true>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = pair_config<T>(2, nullptr, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    return n;
+  }
 }
 
 template <class T>
@@ -1042,11 +1246,17 @@ using TraitsD128 = Tc05Traits<128, 0, 128, false>;
 using TraitsD128R64 = Tc05Traits<128, 64, 128, false>;
 using TraitsFp8D128 = Tc05Traits<128, 0, 128, true>;
 using TraitsFp8QkvD128 = Tc05Traits<128, 0, 128, true, true>;
+using TraitsD128Pair = Tc05Traits<128, 0, 128, false, false, true>;
+using TraitsD128R64Pair = Tc05Traits<128, 64, 128, false, false, true>;
 
 cudaError_t tc05_launch_d64(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
 cudaError_t tc05_launch_d128(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
 cudaError_t tc05_launch_d128r64(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
 cudaError_t tc05_launch_fp8d128(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
 cudaError_t tc05_launch_fp8qkvd128(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
+cudaError_t tc05_launch_d128pair(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
+cudaError_t tc05_launch_d128r64pair(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
+int tc05_max_clusters_d128pair();
+int tc05_max_clusters_d128r64pair();
 
 }  // namespace af

@@ -8,7 +8,8 @@
 
 namespace af {
 
-constexpr int kRowsPerTile = 256;   // query rows per work tile of the tcgen05 kernel
+constexpr int kRowsPerTile = 256;   // query rows per work tile of the tcgen05 kernel (one CTA)
+constexpr int kRowsPerTilePair = 512;   // the same for a CTA pair (two M = 256 MMA tiles)
 constexpr int kBlockM = 128;        // query rows per MMA tile (one TMEM lane per row)
 constexpr int kBlockN = 128;        // keys per K/V tile
 constexpr int64_t kL2ChunkBudget = 48ll << 20;   // K/V bytes one scheduling chunk may keep in L2
@@ -47,7 +48,8 @@ struct Tc05Params {
   uint32_t* ws;            // workspace words
   int64_t o_stride_b, o_stride_t, o_stride_h;  // elements
   int32_t batch, seqlen_q, seqlen_k, heads_q, heads_kv, group;
-  int32_t tiles_per_seq;   // fixed length: ceil(Sq / kRowsPerTile)
+  int32_t tiles_per_seq;   // fixed length: ceil(Sq / rows_per_tile)
+  int32_t rows_per_tile;   // query rows per work tile (kRowsPerTile, or kRowsPerTilePair for CTA pairs)
   int32_t kv_chunk;        // KV heads per scheduling chunk
   int64_t total_work;      // fixed length: exact number of work tiles
   int32_t packed;
@@ -81,7 +83,9 @@ enum Tc05Variant : int {
   kVarD128Rope64 = 2, // bf16, Dqk = 128 + rope 64, Dv = 128
   kVarFp8D128 = 3,    // fp8 e4m3 Q/K, Dqk = Dv = 128
   kVarFp8QkvD128 = 4, // fp8 e4m3 Q/K/V (depth-major V, P rounded to e4m3), Dqk = Dv = 128
-  kVarCount = 5
+  kVarD128Pair = 5,   // kVarD128 on CTA pairs (M = 256 MMAs over two CTAs)
+  kVarD128Rope64Pair = 6, // kVarD128Rope64 on CTA pairs
+  kVarCount = 7
 };
 
 struct Tc05Config {
@@ -98,8 +102,13 @@ attn_status report_error(attn_status st, const char* fmt, ...);
 
 // Static configuration of a variant (host).
 Tc05Config tc05_config(int variant);
-// Launch of one variant (defined in the per-variant translation units).
+// Launch of one variant (defined in the per-variant translation units); a
+// pair variant's grid counts CTAs and must be even.
 cudaError_t tc05_launch(int variant, bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
+// Pair variants: clusters of two CTAs that fit on the current device at once
+// (0 when unknown).
+int tc05_max_clusters(int variant);
+inline bool tc05_is_pair(int variant) { return variant == kVarD128Pair || variant == kVarD128Rope64Pair; }
 // Launch of the split-KV merge kernel (head_dim_v 64 or 128).
 cudaError_t splitkv_combine_launch(const SplitCombineParams& p, int head_dim_v, cudaStream_t stream);
 // Launch of the plain CUDA-core kernel.

@@ -9,6 +9,8 @@ Tc05Config tc05_config(int variant) {
     case kVarD128: return tc05_config_t<TraitsD128>();
     case kVarD128Rope64: return tc05_config_t<TraitsD128R64>();
     case kVarFp8QkvD128: return tc05_config_t<TraitsFp8QkvD128>();
+    case kVarD128Pair: return tc05_config_t<TraitsD128Pair>();
+    case kVarD128Rope64Pair: return tc05_config_t<TraitsD128R64Pair>();
     default: return tc05_config_t<TraitsFp8D128>();
   }
 }
@@ -20,7 +22,17 @@ cudaError_t tc05_launch(int variant, bool causal, const Tc05Params& prm, int gri
     case kVarD128Rope64: return tc05_launch_d128r64(causal, prm, grid, stream);
     case kVarFp8D128: return tc05_launch_fp8d128(causal, prm, grid, stream);
     case kVarFp8QkvD128: return tc05_launch_fp8qkvd128(causal, prm, grid, stream);
+    case kVarD128Pair: return tc05_launch_d128pair(causal, prm, grid, stream);
+    case kVarD128Rope64Pair: return tc05_launch_d128r64pair(causal, prm, grid, stream);
     default: return cudaErrorInvalidValue;
+  }
+}
+
+int tc05_max_clusters(int variant) {
+  switch (variant) {
+    case kVarD128Pair: return tc05_max_clusters_d128pair();
+    case kVarD128Rope64Pair: return tc05_max_clusters_d128r64pair();
+    default: return 0;
   }
 }
 

@@ -77,6 +77,19 @@ typedef enum attn_schedule {
                                    in index order as SMs free up */
 } attn_schedule;
 
+/* CTA pairs (the "pair_cta" option of the SM100AttentionSMem page's barrier
+ * set, FA4MiscMBars): two CTAs of a cluster on neighbouring SMs share every
+ * tensor-core instruction (M = 256 rows, tcgen05 cta_group::2). Each CTA
+ * holds 128 of the rows of an instruction, half of every K tile (64 keys) and
+ * half of every V tile (64 depth columns), so each SM reads and stages half
+ * the K/V bytes; a work tile is 512 query rows. Results are those of the
+ * one-CTA kernel (same arithmetic per row). */
+typedef enum attn_pair_cta {
+  ATTN_PAIR_AUTO = 0,           /* the library chooses */
+  ATTN_PAIR_OFF = 1,            /* one CTA per MMA tile */
+  ATTN_PAIR_ON = 2              /* CTA pairs: bf16 Q/K/V, Dqk = Dv = 128, rope 0 or 64; tcgen05 backend */
+} attn_pair_cta;
+
 /* Bytes of workspace attn_fwd needs without split-KV; the workspace holds the
  * persistent scheduler's work counter and the device error record (and, with
  * split-KV, the partial results: see attn_fwd_workspace_bytes). */
@@ -153,20 +166,26 @@ typedef struct attn_fwd_params {
 
   /* attn_schedule; ignored by the simple backend. */
   int32_t schedule;
+
+  /* attn_pair_cta. ATTN_PAIR_ON outside its supported configurations (see
+   * attn_pair_cta) is UNSUPPORTED; with it fault_injection must be 0. */
+  int32_t pair_cta;
 } attn_fwd_params;
 
 /* Query results of attn_fwd_plan (host only; no GPU needed). */
 typedef struct attn_fwd_plan_info {
   int32_t backend;          /* kernel that attn_fwd would launch */
-  int32_t rows_per_tile;    /* query rows per work tile */
+  int32_t rows_per_tile;    /* query rows per work tile (256; 512 with CTA pairs) */
   int64_t work_tiles;       /* fixed: exact count; packed: upper bound B*Hq*ceil(Sq/rows) */
-  int32_t grid;             /* CTAs launched (persistent: min(SMs, work_tiles)) */
+  int32_t grid;             /* CTAs launched (persistent: min(SMs, work_tiles); CTA pairs:
+                               2 * min(resident clusters, work_tiles)) */
   int32_t block;            /* threads per CTA */
   int32_t smem_bytes;       /* dynamic shared memory per CTA */
   int32_t k_stages;         /* depth of the K ring */
   int32_t v_stages;         /* depth of the V ring */
   int32_t tmem_columns;     /* tensor-memory columns allocated per CTA */
   int32_t num_splits;       /* key ranges per query tile (1 = no split-KV) */
+  int32_t pair_cta;         /* 1 = one CTA per MMA tile, 2 = CTA pairs */
 } attn_fwd_plan_info;
 
 /* One work tile as the persistent scheduler hands it out. */

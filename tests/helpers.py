@@ -76,7 +76,7 @@ def assert_within(err, dtype):
         assert err[key] <= bound, f"{key}={err[key]:.3e} exceeds {bound:.1e} ({err})"
 
 
-def run_lib(inputs, backend="tcgen05", device="cuda", num_splits=0):
+def run_lib(inputs, backend="tcgen05", device="cuda", num_splits=0, **kw):
     """Runs the library on a workload input dict; returns (O, LSE) as CPU tensors."""
     import attention_forward_sm100_gb300 as pkg
     spec = inputs["spec"]
@@ -88,14 +88,14 @@ def run_lib(inputs, backend="tcgen05", device="cuda", num_splits=0):
                          q_rope=d.get("q_rope"), k_rope=d.get("k_rope"), q_scale=d.get("q_scale"),
                          k_scale=d.get("k_scale"), cu_seqlens_q=d.get("cu_seqlens_q"),
                          cu_seqlens_k=d.get("cu_seqlens_k"), max_seqlen_q=max(lq + [0]),
-                         max_seqlen_k=max(lk + [0]), backend=backend, num_splits=num_splits)
+                         max_seqlen_k=max(lk + [0]), backend=backend, num_splits=num_splits, **kw)
     pkg.check(device=dev)
     return o.cpu(), lse.cpu()
 
 
-def compare_full(inputs, backend="tcgen05"):
+def compare_full(inputs, backend="tcgen05", **kw):
     """Element-wise errors of the library against the full oracle."""
-    o, lse = run_lib(inputs, backend)
+    o, lse = run_lib(inputs, backend, **kw)
     o_ref, lse_ref = run_oracle(inputs)
     return errors(f64(o), o_ref, lse.double().numpy(), lse_ref)
 

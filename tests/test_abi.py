@@ -378,3 +378,87 @@ def test_binding_refuses_inconsistent_shapes(pkg, case):
         kw.update(cu_seqlens_q=m(3, dt=torch.int64), cu_seqlens_k=m(3, dt=torch.int64))
     with pytest.raises(ValueError):
         pkg.make_params(q, k, v, causal=False, **kw)
+
+
+# ---------------------------------------------------------------- CTA pairs
+def test_pair_plan(pkg):
+    p = _params(pkg, B=4, S=4096, Hq=16, Hkv=16, pair_cta="on")
+    info = pkg.plan(p)
+    assert info.pair_cta == 2 and info.rows_per_tile == 512
+    assert info.work_tiles == 4 * 16 * 8
+    assert info.grid % 2 == 0 and 2 <= info.grid <= 2 * info.work_tiles
+    assert 0 < info.smem_bytes <= 232448
+    # more K and V stages than the one-CTA kernel: each holds half a tile
+    one = pkg.plan(_params(pkg, B=4, S=4096, Hq=16, Hkv=16, pair_cta="off"))
+    assert one.pair_cta == 1 and one.rows_per_tile == 256
+    assert info.k_stages > one.k_stages and info.v_stages > one.v_stages
+    # the library's own choice keeps one CTA per MMA tile
+    assert pkg.plan(_params(pkg, B=4, S=4096, Hq=16, Hkv=16)).pair_cta == 1
+    # one cluster per work tile when the grid schedule is asked for
+    g = pkg.plan(_params(pkg, B=1, S=1000, Hq=2, Hkv=2, pair_cta="on", schedule="grid"))
+    assert g.work_tiles == 2 * 2 and g.grid == 2 * g.work_tiles
+
+
+def test_pair_plan_rope(pkg):
+    q = _Fake((2, 4096, 128, 128), ptr=1 << 20)
+    k = _Fake((2, 4096, 128, 128), ptr=2 << 20)
+    v = _Fake((2, 4096, 128, 128), ptr=3 << 20)
+    o = _Fake((2, 4096, 128, 128), ptr=4 << 20)
+    qr = _Fake((2, 4096, 128, 64), ptr=6 << 20)
+    kr = _Fake((2, 4096, 64), ptr=7 << 20)
+    ws = _Fake((256,), dtype=torch.uint8, ptr=5 << 20)
+    p = pkg.make_params(q, k, v, causal=True, out=o, q_rope=qr, k_rope=kr, workspace=ws, pair_cta="on")
+    info = pkg.plan(p)
+    assert info.pair_cta == 2 and info.rows_per_tile == 512 and info.smem_bytes <= 232448
+    assert info.k_stages >= 3 and info.v_stages >= 3
+
+
+@pytest.mark.parametrize("case,status", [("d64", 2), ("fp8", 2), ("simple", 2), ("fault", 2), ("value", 1)])
+def test_pair_rejections(pkg, case, status):
+    if case == "d64":
+        p = _params(pkg, D=64, Dv=64, pair_cta="on")
+    elif case == "fp8":
+        q = _Fake((1, 256, 2, 128), dtype=torch.float8_e4m3fn, ptr=1 << 20)
+        k = _Fake((1, 256, 2, 128), dtype=torch.float8_e4m3fn, ptr=2 << 20)
+        v = _Fake((1, 256, 2, 128), ptr=3 << 20)
+        o = _Fake((1, 256, 2, 128), ptr=4 << 20)
+        qs = _Fake((1, 2, 256), dtype=torch.float32, ptr=6 << 20)
+        ks = _Fake((1, 2, 256), dtype=torch.float32, ptr=7 << 20)
+        ws = _Fake((256,), dtype=torch.uint8, ptr=5 << 20)
+        p = pkg.make_params(q, k, v, causal=True, out=o, q_scale=qs, k_scale=ks, workspace=ws, pair_cta="on")
+    elif case == "simple":
+        p = _params(pkg, pair_cta="on", backend="simple")
+    elif case == "fault":
+        p = _params(pkg, pair_cta="on")
+        p.fault_injection = 1
+    else:
+        p = _params(pkg)
+        p.pair_cta = 3
+    with pytest.raises(pkg.AttnError) as e:
+        pkg.plan(p)
+    assert e.value.status == status
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv", [(1, 1, 1, 1), (2, 700, 8, 2), (1, 4096, 16, 16)])
+def test_pair_schedule_covers_each_tile_once(pkg, B, S, Hq, Hkv):
+    p = _params(pkg, B=B, S=S, Hq=Hq, Hkv=Hkv, pair_cta="on")
+    order = pkg.schedule(p)
+    T = (S + 511) // 512
+    assert len(order) == B * Hq * T
+    assert set(order) == {(b, h, t) for b in range(B) for h in range(Hq) for t in range(T)}
+    g = Hq // Hkv
+    for b in range(B):
+        for hk in range(Hkv):
+            seq = [t for (bb, h, t) in order if bb == b and h // g == hk]
+            assert seq == sorted(seq, reverse=True)
+
+
+def test_pair_schedule_packed(pkg):
+    lens = [2646, 7628, 1356, 5009, 4477, 3351, 2296, 891]
+    cu = [0]
+    for n in lens:
+        cu.append(cu[-1] + n)
+    p = _params(pkg, B=8, S=8192, Hq=32, Hkv=8, pair_cta="on")
+    order = pkg.schedule(p, host_cu_seqlens_q=cu)
+    expect = {(b, h, t) for b, n in enumerate(lens) for h in range(32) for t in range((n + 511) // 512)}
+    assert len(order) == len(expect) and set(order) == expect
