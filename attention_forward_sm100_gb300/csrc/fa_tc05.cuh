@@ -85,7 +85,8 @@ enum BarId : int {
   BAR_Q_EMPTY1 = 26,     // last S MMA of Q tile 1 done
   BAR_WORK_FULL = 27,    // +slot, CTA pairs: work index written into the second CTA by the first
   BAR_WORK_EMPTY = 29,   // +slot, CTA pairs: the second CTA read that work index
-  BAR_FIXED = 31         // then K_FULL[NK], K_EMPTY[NK], V_FULL[NV], V_EMPTY[NV]
+  BAR_SM_TURN = 31,      // +i, softmax turn of warpgroup i (128 arrivals of the other warpgroup)
+  BAR_FIXED = 33         // then K_FULL[NK], K_EMPTY[NK], V_FULL[NV], V_EMPTY[NV]
 };
 
 constexpr int kSlotBytes = 48;   // shared-memory bytes of one SchedSlot entry
@@ -173,6 +174,12 @@ struct Tc05Traits {
   // epilogue warpgroup then fits in 64 (measured: +1-3 % on the FP8
   // workloads, no change for bf16).
   static constexpr int REG_SOFTMAX = FP8 ? 192 : 184, REG_CORR = FP8 ? 64 : 80, REG_MISC = 64;
+  // Softmax turn: 0 = the two softmax warpgroups run freely; 1 / 2 = they
+  // take turns, handing over after the first half of P / after the tile.
+  // With FP8 Q/K a tile's MMAs take less time than a softmax, and two
+  // softmaxes that overlap each take twice as long: taking turns keeps them
+  // apart.
+  static constexpr int SM_TURN = FP8 ? 1 : 0;
   static_assert(2 * 128 * REG_SOFTMAX + 128 * REG_CORR + 128 * REG_MISC <= 512 * 128,
                 "register split exceeds the launch allocation");
 };
@@ -260,6 +267,14 @@ __device__ __forceinline__ bool wait_drain(const Ctx& c, int id, uint32_t parity
     if (ptx::globaltimer() - t0 > kDrainTimeoutNs) return false;
   }
   return true;
+}
+
+// CTA pairs: arrival on barrier `id` of the pair's first CTA (a local arrive
+// there, a release at cluster scope through the cluster window from the
+// second CTA).
+__device__ __forceinline__ void arrive_lead(const Ctx& c, int id) {
+  if (c.rank == 0) ptx::mbar_arrive(c.bar(id));
+  else ptx::mbar_arrive_cluster(c.bar_lead(id));
 }
 
 // Ring position: stage index and phase parity.
@@ -774,7 +789,8 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
   float* ks_sm = reinterpret_cast<float*>(c.smem + T::OFF_KS) + i * 2 * kBlockN;
   const int role = i == 0 ? kRoleSoftmax0 : kRoleSoftmax1;
   Ring<2> sched;
-  uint32_t s_phase = 0, ks_phase = 0, stats_phase = 0;
+  uint32_t s_phase = 0, ks_phase = 0, stats_phase = 0, turn_phase = 0;
+  const uint32_t turn_flip = i == 0 ? 1u : 0u;   // warpgroup 0 takes the first turn
   while (true) {
     if (!wait_warp(c, BAR_SCHED_FULL + sched.idx, sched.phase, role)) return;
     const SchedSlot s = read_slot(c, sched.idx, T::OFF_SCHED);
@@ -820,6 +836,10 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
       }
       if (!wait_warp(c, BAR_S_FULL + i, s_phase, role)) return;
       s_phase ^= 1u;
+      if (T::SM_TURN) {
+        if (!wait_warp(c, BAR_SM_TURN + i, turn_phase ^ turn_flip, role)) return;
+        turn_phase ^= 1u;
+      }
       ptx::tc_fence_after();
       float sv[128];
       {
@@ -917,16 +937,25 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
         if constexpr (T::PAIR) {
           // one arrival per warp on the first CTA's barrier
           __syncwarp();
-          if ((threadIdx.x & 31) == 0) ptx::mbar_arrive_cluster(c.bar_lead((half == 0 ? BAR_P_LO : BAR_P_HI) + i));
+          if ((threadIdx.x & 31) == 0) arrive_lead(c, (half == 0 ? BAR_P_LO : BAR_P_HI) + i);
         } else {
           ptx::mbar_arrive(c.bar((half == 0 ? BAR_P_LO : BAR_P_HI) + i));
         }
+        if (T::SM_TURN == half + 1) ptx::mbar_arrive(c.bar(BAR_SM_TURN + (i ^ 1)));   // the other warpgroup's turn
       }
       float s0, s1, s2, s3;
       ptx::f2_unpack(acc0, s0, s1);
       ptx::f2_unpack(acc1, s2, s3);
       l = l * alpha + ((s0 + s1) + (s2 + s3));
       m = m_use;
+    }
+    if (T::SM_TURN) {
+      // K/V tiles only the other Q tile visits: pass the turn on.
+      for (int j = n; j < g.n[1]; ++j) {
+        if (!wait_warp(c, BAR_SM_TURN + i, turn_phase ^ turn_flip, role)) return;
+        turn_phase ^= 1u;
+        ptx::mbar_arrive(c.bar(BAR_SM_TURN + (i ^ 1)));
+      }
     }
     // Row statistics: LSE (natural log) here, 1/l to the epilogue. A split-KV
     // range writes the LSE of its own keys for the merge.
@@ -1035,7 +1064,7 @@ __device__ void role_correction(const Tc05Params& P, const Ctx& c) {
       if constexpr (T::PAIR) {
         // one arrival per warp on the first CTA's barrier (its MMAs write both CTAs' O)
         __syncwarp();
-        if ((threadIdx.x & 31) == 0) ptx::mbar_arrive_cluster(c.bar_lead(BAR_O_FREE + i));
+        if ((threadIdx.x & 31) == 0) arrive_lead(c, BAR_O_FREE + i);
       } else {
         ptx::mbar_arrive(c.bar(BAR_O_FREE + i));
       }
@@ -1090,6 +1119,7 @@ __global__ void __launch_bounds__(512, 1) fa_tc05_kernel(const __grid_constant__
       ptx::mbar_init(c.bar(BAR_SCHED_EMPTY + i), kSchedConsumers - (c.rank != 0 ? 2u : 0u));
       ptx::mbar_init(c.bar(BAR_WORK_FULL + i), 1);
       ptx::mbar_init(c.bar(BAR_WORK_EMPTY + i), 1);
+      ptx::mbar_init(c.bar(BAR_SM_TURN + i), 128);
     }
     ptx::mbar_init(c.bar(BAR_Q_EMPTY), 1);
     ptx::mbar_init(c.bar(BAR_Q_EMPTY1), 1);
