@@ -314,6 +314,56 @@ def forward(q, k, v, *, causal=False, softmax_scale=None, q_rope=None, k_rope=No
     return out, lse
 
 
+class PreparedForward:
+    """A forward whose tensors, options and workspace stay fixed across calls
+    (a serving loop that refills the same buffers): the parameter struct is
+    marshalled once, and each ``run`` is one ``attn_fwd`` call (the library
+    reuses the tensor maps it encoded for the same tensors). Build it with
+    ``prepare`` (same arguments as ``forward``); ``out`` and ``lse`` hold the
+    results of the latest run."""
+
+    def __init__(self, q, k, v, **kw):
+        for name in ("q", "k", "v"):
+            _require_cuda(name, locals()[name])
+        stream = kw.pop("stream", None)
+        dev = q.device
+        packed = kw.get("cu_seqlens_q") is not None
+        if kw.get("out") is None:
+            kw["out"] = torch.empty(q.shape[:-1] + (head_dim_v(v),), dtype=torch.bfloat16, device=dev)
+        if kw.get("lse") is None:
+            shape = (q.shape[1], q.shape[0]) if packed else (q.shape[0], q.shape[2], q.shape[1])
+            kw["lse"] = torch.empty(shape, dtype=torch.float32, device=dev)
+        for name in ("q_rope", "k_rope", "q_scale", "k_scale", "cu_seqlens_q", "cu_seqlens_k"):
+            _require_cuda(name, kw.get(name))
+        self.out, self.lse = kw["out"], kw["lse"]
+        self._keep = (q, k, v, kw)   # the tensors must outlive the prepared call
+        self._p = make_params(q, k, v, **kw)
+        ws = kw.get("workspace")
+        if ws is None:
+            with torch.cuda.device(dev):
+                need = workspace_bytes(self._p)
+            ws = default_workspace(dev, need)
+            self._p.workspace, self._p.workspace_bytes = ws.data_ptr(), ws.numel()
+        self.workspace = ws
+        self._ref = ctypes.byref(self._p)
+        self._fn = lib().attn_fwd
+        self._stream = stream if stream is not None else torch.cuda.current_stream(dev)
+        self._handle = ctypes.c_void_p(self._stream.cuda_stream if hasattr(self._stream, "cuda_stream")
+                                       else int(self._stream))
+
+    def run(self):
+        """Enqueues the forward on the stream given at preparation."""
+        st = self._fn(self._ref, self._handle)
+        if st != ATTN_OK:
+            raise AttnError(st, last_error())
+        return self.out, self.lse
+
+
+def prepare(q, k, v, **kw) -> PreparedForward:
+    """A ``PreparedForward`` for fixed tensors and options (see ``forward``)."""
+    return PreparedForward(q, k, v, **kw)
+
+
 def check(workspace=None, device=None, stream=None):
     """Synchronises and raises if a kernel wait ran out of time."""
     L = lib()

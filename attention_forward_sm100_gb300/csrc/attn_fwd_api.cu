@@ -165,7 +165,10 @@ int tc05_variant(const attn_fwd_params* p) {
 }
 
 // Query rows of one work tile.
-int32_t rows_for(const attn_fwd_params* p) { return use_pair(p) ? af::kRowsPerTilePair : af::kRowsPerTile; }
+int32_t rows_for(const attn_fwd_params* p) {
+  if (p->backend == ATTN_BACKEND_TCGEN05 && af::tc05_is_rowsplit(tc05_variant(p))) return af::kRowsPerTileRs;
+  return use_pair(p) ? af::kRowsPerTilePair : af::kRowsPerTile;
+}
 
 int sm_count_cached() {
   static std::atomic<int> cache[64];
@@ -281,6 +284,55 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Encoded 4-D maps of the calling thread's recent calls, so a call that
+// repeats another one's tensors (a serving loop, a benchmark) skips the
+// driver's encoder. The key holds every encoder argument; a map depends on
+// nothing else, so a hit is exact.
+struct MapKey {
+  const void* base;
+  int dt;
+  cuuint64_t dims[4];
+  cuuint64_t strides[3];
+  cuuint32_t box[4];
+};
+struct MapEntry {
+  MapKey key;
+  CUtensorMap map;
+  bool used;
+};
+constexpr int kMapCacheEntries = 16;
+thread_local MapEntry g_map_cache[kMapCacheEntries];
+thread_local int g_map_cache_next = 0;
+
+CUresult encode_4d_cached(EncodeTiledFn fn, CUtensorMap* map, CUtensorMapDataType dt, const void* base,
+                          const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box) {
+  MapKey key;
+  memset(&key, 0, sizeof(key));
+  key.base = base;
+  key.dt = (int)dt;
+  memcpy(key.dims, dims, sizeof(key.dims));
+  memcpy(key.strides, strides, sizeof(key.strides));
+  memcpy(key.box, box, sizeof(key.box));
+  for (int i = 0; i < kMapCacheEntries; ++i) {
+    if (g_map_cache[i].used && memcmp(&g_map_cache[i].key, &key, sizeof(key)) == 0) {
+      *map = g_map_cache[i].map;
+      return CUDA_SUCCESS;
+    }
+  }
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  const CUresult r = fn(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r == CUDA_SUCCESS) {
+    MapEntry& e = g_map_cache[g_map_cache_next];
+    g_map_cache_next = (g_map_cache_next + 1) % kMapCacheEntries;
+    e.key = key;
+    e.map = *map;
+    e.used = true;
+  }
+  return r;
+}
+
 // 4-D map over (depth, head, token, batch); box {box_d, 1, box_rows, 1}, 128-byte swizzle.
 attn_status make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int es, int64_t depth,
                      int64_t heads, int64_t tokens, int64_t batches, int64_t sh, int64_t st, int64_t sb,
@@ -293,10 +345,7 @@ attn_status make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt,
   cuuint64_t dims[4] = {(cuuint64_t)depth, (cuuint64_t)heads, (cuuint64_t)tokens, (cuuint64_t)batches};
   cuuint64_t strides[3] = {(cuuint64_t)(sh * es), (cuuint64_t)(st * es), (cuuint64_t)(sb * es)};
   cuuint32_t box[4] = {(cuuint32_t)box_d, 1u, (cuuint32_t)box_rows, 1u};
-  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-  CUresult r = fn(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = encode_4d_cached(fn, map, dt, base, dims, strides, box);
   if (r != CUDA_SUCCESS)
     return fail(ATTN_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (%d) for a %lldx%lldx%lldx%lld tensor", (int)r,
                 (long long)depth, (long long)heads, (long long)tokens, (long long)batches);
@@ -317,10 +366,7 @@ attn_status make_map_vt(CUtensorMap* map, const attn_fwd_params* p, const void* 
                         (cuuint64_t)p->batch};
   cuuint64_t strides[3] = {(cuuint64_t)sd, (cuuint64_t)sh, (cuuint64_t)sb};
   cuuint32_t box[4] = {(cuuint32_t)af::kBlockN, (cuuint32_t)p->head_dim_v, 1u, 1u};
-  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = encode_4d_cached(fn, map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, dims, strides, box);
   if (r != CUDA_SUCCESS) return fail(ATTN_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (%d) for fp8 V", (int)r);
   return ATTN_OK;
 }

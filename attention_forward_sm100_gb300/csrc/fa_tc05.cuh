@@ -55,6 +55,8 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <atomic>
+
 #include "internal.h"
 #include "ptx.cuh"
 #include "schedule.cuh"
@@ -1220,21 +1222,54 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribut
   return cfg;
 }
 
+// Raises a kernel's dynamic shared-memory limit once per device (the
+// attribute stays set for the life of the context); `force` sets it again
+// (after a context was torn down and recreated).
+template <auto KERN>
+cudaError_t set_smem_once(int bytes, bool force = false) {
+  static std::atomic<uint64_t> done{0};   // one per kernel
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (!force && bit != 0ull && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(KERN, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0ull) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+// Launches `launch()`; if that fails, sets the kernel's shared-memory limit
+// again and retries once.
+template <auto KERN, class F>
+cudaError_t launch_with_smem(int bytes, F launch) {
+  cudaError_t e = set_smem_once<KERN>(bytes);
+  if (e != cudaSuccess) return e;
+  e = launch();
+  if (e == cudaSuccess) return e;
+  if ((e = set_smem_once<KERN>(bytes, true)) != cudaSuccess) return e;
+  return launch();
+}
+
+template <class T, bool CAUSAL>
+cudaError_t tc05_launch_tc(const Tc05Params& prm, int grid, cudaStream_t stream) {
+  constexpr auto kern = fa_tc05_kernel<T, CAUSAL>;
+  return launch_with_smem<kern>(T::SMEM_BYTES, [&]() -> cudaError_t {
+    if constexpr (T::PAIR) {
+      if (grid % 2 != 0) return cudaErrorInvalidValue;
+      cudaLaunchAttribute attr[1];
+      const cudaLaunchConfig_t cfg = pair_config<T>(grid, stream, attr);
+      const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm);
+      if (e != cudaSuccess) return e;
+    } else {
+      kern<<<grid, 512, T::SMEM_BYTES, stream>>>(prm);
+    }
+    return cudaGetLastError();
+  });
+}
+
 template <class T>
 cudaError_t tc05_launch_t(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream) {
-  auto kern = causal ? fa_tc05_kernel<T, true> : fa_tc05_kernel<T, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  if constexpr (T::PAIR) {
-    if (grid % 2 != 0) return cudaErrorInvalidValue;
-    cudaLaunchAttribute attr[1];
-    const cudaLaunchConfig_t cfg = pair_config<T>(grid, stream, attr);
-    e = cudaLaunchKernelEx(&cfg, kern, prm);
-    if (e != cudaSuccess) return e;
-  } else {
-    kern<<<grid, 512, T::SMEM_BYTES, stream>>>(prm);
-  }
-  return cudaGetLastError();
+  return causal ? tc05_launch_tc<T, true>(prm, grid, stream) : tc05_launch_tc<T, false>(prm, grid, stream);
 }
 
 // Clusters of a pair variant that can be resident at once on the current

@@ -319,6 +319,48 @@ def soak(step, dev, seconds):
         torch.cuda.synchronize(dev)
 
 
+def small_call_latency(d, kw, stream, dev, calls=2000):
+    """Per-call times of a problem small enough to be bound by the host path:
+    back-to-back calls through ``forward`` (marshalling every call) and
+    through a prepared call (``prepare``: one attn_fwd per call), wall time
+    over `calls` calls; and the same call captured 100 times in a CUDA graph
+    and replayed."""
+    import torch
+
+    import attention_forward_sm100_gb300 as pkg
+    out = {}
+    prep = pkg.prepare(d["q"], d["k"], d["v"], stream=stream, **kw)
+    for name, fn in (("forward_us_per_call", lambda: pkg.forward(d["q"], d["k"], d["v"], stream=stream, **kw)),
+                     ("prepared_us_per_call", prep.run)):
+        for _ in range(50):
+            fn()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(calls):
+            fn()
+        torch.cuda.synchronize(dev)
+        out[name] = (time.perf_counter() - t0) * 1e6 / calls
+    pkg.check(device=dev)
+    g = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream(dev)
+    cs.wait_stream(stream)
+    with torch.cuda.graph(g, stream=cs):
+        for _ in range(100):
+            pkg.forward(d["q"], d["k"], d["v"], stream=cs, **kw)
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(cs):          # replay() launches on the current stream
+        g.replay()
+        torch.cuda.synchronize(dev)
+        g0.record(cs)
+        for _ in range(5):
+            g.replay()
+        g1.record(cs)
+    torch.cuda.synchronize(dev)
+    out["graph_replay_us_per_call"] = g0.elapsed_time(g1) * 1e3 / 500
+    pkg.check(device=dev)
+    return out
+
+
 def peak_label(spec, peak_src):
     if spec.v_dtype == "fp8":
         return f"2 x bf16 burst (fp8 Q/K/V), {peak_src}"
@@ -368,6 +410,7 @@ def time_other_workloads(args, dev, stream, peaks, peak_src):
             med = statistics.median(per_call)
             entry["us_per_call"] = med * 1e3
             entry["algorithmic_gbs"] = spec.hbm_bytes() / (med * 1e-3) / 1e9
+            entry["latency"] = small_call_latency(d, kw, stream, dev)
         res[name] = entry
         del inputs, d, kw, out, lse
         torch.cuda.empty_cache()
@@ -461,27 +504,9 @@ def main():
     peaks, peak_src = load_peaks()
     peak = peak_tflops(spec, peaks)
 
-    # A problem this small is bound by the host's launch path: also time the
-    # same call captured once in a CUDA graph and replayed (100 calls per replay).
-    graph_us = None
-    if spec.flops() < 1e10:
-        g = torch.cuda.CUDAGraph()
-        cs = torch.cuda.Stream(dev)
-        cs.wait_stream(stream)
-        with torch.cuda.graph(g, stream=cs):
-            for _ in range(100):
-                pkg.forward(d["q"], d["k"], d["v"], stream=cs, **kw)
-        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(cs):          # replay() launches on the current stream
-            g.replay()
-            torch.cuda.synchronize(dev)
-            g0.record(cs)
-            for _ in range(5):
-                g.replay()
-            g1.record(cs)
-        torch.cuda.synchronize(dev)
-        graph_us = g0.elapsed_time(g1) * 1e3 / 500
-        pkg.check(device=dev)
+    # A problem this small is bound by the host's launch path: also time it
+    # through a prepared call and replayed from a CUDA graph.
+    small = small_call_latency(d, kw, stream, dev) if spec.flops() < 1e10 else None
 
     e2e = None
     if not args.no_e2e:
@@ -590,9 +615,9 @@ def main():
         if flops < 1e10:
             # a problem this small is bound by launch latency, not by the tensor cores
             hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-            line["latency"] = {"us_per_call": median_ms * 1e3,
-                               "algorithmic_gbs": spec.hbm_bytes() / (median_ms * 1e-3) / 1e9,
-                               "hbm_peak_gbs": hbm, "graph_replay_us_per_call": graph_us}
+            line["latency"] = dict({"us_per_call": median_ms * 1e3,
+                                    "algorithmic_gbs": spec.hbm_bytes() / (median_ms * 1e-3) / 1e9,
+                                    "hbm_peak_gbs": hbm}, **small)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

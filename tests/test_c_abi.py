@@ -56,3 +56,31 @@ def test_c_program_runs_forward_on_gpu(lib_dir, tmp_path):
     print(r.stdout)
     assert r.returncode == 0, r.stdout + r.stderr
     assert r.stdout.strip().endswith("ok")
+
+
+@pytest.mark.gpu
+def test_c_host_cost(lib_dir, tmp_path):
+    """A C caller's host time per attn_fwd call on the 128-token workload
+    shape (the number is printed; the bound only catches a gross
+    regression such as re-encoding every tensor map through a slow path)."""
+    cc = shutil.which("gcc") or shutil.which("cc")
+    cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    if cc is None or not os.path.exists(os.path.join(cuda, "include", "cuda_runtime.h")):
+        pytest.skip("no C compiler or CUDA headers")
+    exe = str(tmp_path / "host_cost")
+    libdirs = [d for d in (os.path.join(cuda, "lib64"), os.path.join(cuda, "lib")) if os.path.isdir(d)]
+    cmd = [cc, "-std=c99", "-O2", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), "-I",
+           os.path.join(cuda, "include"), os.path.join(ROOT, "tests", "c", "host_cost.c"), "-L", lib_dir,
+           "-lattn_fwd", "-Wl,-rpath," + lib_dir]
+    for d in libdirs:
+        cmd += ["-L", d, "-Wl,-rpath," + d]
+    cmd += ["-lcudart", "-o", exe]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=300)
+    print(r.stdout)
+    assert r.returncode == 0, r.stdout + r.stderr
+    fields = r.stdout.split()
+    assert fields[-1] == "ok"
+    enqueue_us = float(fields[fields.index("enqueue_us") + 1])
+    assert enqueue_us < 50.0
