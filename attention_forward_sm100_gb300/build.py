@@ -26,7 +26,7 @@ LIB_PATH = os.path.join(HERE, "libattn_fwd.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
                  "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include")]
-PERSISTENT_KERNEL = "fa_tc05_kernel"
+PERSISTENT_KERNELS = ("fa_tc05_kernel",)
 REGS_EXPECTED = 128
 SPILL_LIMIT = 64   # bytes of local-memory spill tolerated per persistent kernel
 
@@ -53,7 +53,7 @@ def _check_ptxas(log: str, src: str):
     entries = re.split(r"ptxas info\s*: Compiling entry function", log)
     for chunk in entries[1:]:
         name = chunk.split("'")[1] if "'" in chunk else ""
-        if PERSISTENT_KERNEL not in name:
+        if not any(k in name for k in PERSISTENT_KERNELS):
             continue
         m = re.search(r"Used (\d+) registers", chunk)
         spills = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", chunk)

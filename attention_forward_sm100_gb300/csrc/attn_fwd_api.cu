@@ -165,10 +165,7 @@ int tc05_variant(const attn_fwd_params* p) {
 }
 
 // Query rows of one work tile.
-int32_t rows_for(const attn_fwd_params* p) {
-  if (p->backend == ATTN_BACKEND_TCGEN05 && af::tc05_is_rowsplit(tc05_variant(p))) return af::kRowsPerTileRs;
-  return use_pair(p) ? af::kRowsPerTilePair : af::kRowsPerTile;
-}
+int32_t rows_for(const attn_fwd_params* p) { return use_pair(p) ? af::kRowsPerTilePair : af::kRowsPerTile; }
 
 int sm_count_cached() {
   static std::atomic<int> cache[64];

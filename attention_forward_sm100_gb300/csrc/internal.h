@@ -85,9 +85,7 @@ enum Tc05Variant : int {
   kVarFp8QkvD128 = 4, // fp8 e4m3 Q/K/V (depth-major V, P rounded to e4m3), Dqk = Dv = 128
   kVarD128Pair = 5,   // kVarD128 on CTA pairs (M = 256 MMAs over two CTAs)
   kVarD128Rope64Pair = 6, // kVarD128Rope64 on CTA pairs
-  kVarFp8D128Rs = 7,  // fp8 e4m3 Q/K, bf16 V: row-split kernel (one 128-row Q tile, double-buffered S)
-  kVarFp8QkvD128Rs = 8, // fp8 e4m3 Q/K/V: row-split kernel
-  kVarCount = 9
+  kVarCount = 7
 };
 
 struct Tc05Config {
@@ -111,9 +109,6 @@ cudaError_t tc05_launch(int variant, bool causal, const Tc05Params& prm, int gri
 // (0 when unknown).
 int tc05_max_clusters(int variant);
 inline bool tc05_is_pair(int variant) { return variant == kVarD128Pair || variant == kVarD128Rope64Pair; }
-// Row-split variants: one 128-row Q tile per work tile.
-inline bool tc05_is_rowsplit(int variant) { return variant == kVarFp8D128Rs || variant == kVarFp8QkvD128Rs; }
-constexpr int kRowsPerTileRs = 128;
 // Launch of the split-KV merge kernel (head_dim_v 64 or 128).
 cudaError_t splitkv_combine_launch(const SplitCombineParams& p, int head_dim_v, cudaStream_t stream);
 // Launch of the plain CUDA-core kernel.

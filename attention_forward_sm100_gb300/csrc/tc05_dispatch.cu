@@ -1,5 +1,5 @@
 // Variant table of the tcgen05 kernel: static configuration and launch.
-#include "fa_rowsplit.cuh"
+#include "fa_tc05.cuh"
 
 namespace af {
 
@@ -11,8 +11,6 @@ Tc05Config tc05_config(int variant) {
     case kVarFp8QkvD128: return tc05_config_t<TraitsFp8QkvD128>();
     case kVarD128Pair: return tc05_config_t<TraitsD128Pair>();
     case kVarD128Rope64Pair: return tc05_config_t<TraitsD128R64Pair>();
-    case kVarFp8D128Rs: return rs_config_t<RsTraitsFp8>();
-    case kVarFp8QkvD128Rs: return rs_config_t<RsTraitsFp8Qkv>();
     default: return tc05_config_t<TraitsFp8D128>();
   }
 }
@@ -26,8 +24,6 @@ cudaError_t tc05_launch(int variant, bool causal, const Tc05Params& prm, int gri
     case kVarFp8QkvD128: return tc05_launch_fp8qkvd128(causal, prm, grid, stream);
     case kVarD128Pair: return tc05_launch_d128pair(causal, prm, grid, stream);
     case kVarD128Rope64Pair: return tc05_launch_d128r64pair(causal, prm, grid, stream);
-    case kVarFp8D128Rs: return rs_launch_fp8(causal, prm, grid, stream);
-    case kVarFp8QkvD128Rs: return rs_launch_fp8qkv(causal, prm, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -265,10 +265,14 @@ def barrier(world):
 
 # The task's workloads timed after the headline one in the same run (GPU
 # only, no CPU leg): the small non-causal case, packed GQA, MLA with the
-# shared rope part and FP8 Q/K; then the two additions (all-FP8 and split-KV).
-OTHER_WORKLOADS = ("mha_b1_h2_s128_d64_noncausal", "varlen_gqa_b8_hq32_hkv8_d128_causal",
-                   "mla_b2_h128_s4096_d128r64_causal", "fp8_b2_h32_s8192_d128_causal",
-                   "fp8qkv_b2_h32_s8192_d128_causal", "splitkv_b1_hq32_hkv8_sq256_sk32768_d128_noncausal")
+# shared rope part and FP8 Q/K; then the two additions (all-FP8 and split-KV);
+# then the d128 and MLA workloads again on CTA pairs (label "+pairs").
+OTHER_WORKLOADS = (("mha_b1_h2_s128_d64_noncausal", {}), ("varlen_gqa_b8_hq32_hkv8_d128_causal", {}),
+                   ("mla_b2_h128_s4096_d128r64_causal", {}), ("fp8_b2_h32_s8192_d128_causal", {}),
+                   ("fp8qkv_b2_h32_s8192_d128_causal", {}),
+                   ("splitkv_b1_hq32_hkv8_sq256_sk32768_d128_noncausal", {}),
+                   ("mha_b4_h16_s4096_d128_causal", {"pair_cta": "on"}),
+                   ("mla_b2_h128_s4096_d128r64_causal", {"pair_cta": "on"}))
 
 
 def prepare(spec, dev, schedule):
@@ -378,11 +382,13 @@ def time_other_workloads(args, dev, stream, peaks, peak_src):
     import attention_forward_sm100_gb300 as pkg
     from attention_forward_sm100_gb300 import workloads as W
     res = {}
-    for name in OTHER_WORKLOADS:
-        if name == args.workload:
+    for name, opts in OTHER_WORKLOADS:
+        if name == args.workload and not opts:
             continue
+        label = name + ("+pairs" if opts.get("pair_cta") == "on" else "")
         spec = W.WORKLOADS[name]
         inputs, d, kw, out, lse, splits, launches = prepare(spec, dev, args.schedule)
+        kw = dict(kw, **opts)
 
         def step():
             pkg.forward(d["q"], d["k"], d["v"], stream=stream, **kw)
@@ -411,7 +417,7 @@ def time_other_workloads(args, dev, stream, peaks, peak_src):
             entry["us_per_call"] = med * 1e3
             entry["algorithmic_gbs"] = spec.hbm_bytes() / (med * 1e-3) / 1e9
             entry["latency"] = small_call_latency(d, kw, stream, dev)
-        res[name] = entry
+        res[label] = entry
         del inputs, d, kw, out, lse
         torch.cuda.empty_cache()
     return res
