@@ -869,8 +869,13 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
       if (need_mask) {
         const int vis = lim - kb;
 #pragma unroll
-        for (int e = 0; e < 128; ++e)
-          if (e >= vis) sv[e] = -INFINITY;
+        for (int q = 0; q < 4; ++q) {
+          const int vq = min(max(vis - 32 * q, 0), 32);
+          const uint32_t bits = vq >= 32 ? 0xffffffffu : ((1u << vq) - 1u);
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (!((bits >> e) & 1u)) sv[32 * q + e] = -INFINITY;
+        }
       }
       float mx0 = ptx::max3(sv[0], sv[1], sv[2]), mx1 = ptx::max3(sv[3], sv[4], sv[5]);
       float mx2 = ptx::max3(sv[6], sv[7], sv[8]), mx3 = ptx::max3(sv[9], sv[10], sv[11]);
