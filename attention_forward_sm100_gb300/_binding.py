@@ -51,6 +51,7 @@ class Params(ctypes.Structure):
         ("num_splits", ctypes.c_int32),
         ("schedule", ctypes.c_int32),
         ("pair_cta", ctypes.c_int32),
+        ("cu_seqlens_v", ctypes.c_void_p), ("total_v", ctypes.c_int32),
     ]
 
 
@@ -150,7 +151,7 @@ def head_dim_v(v) -> int:
 
 
 def _check_layout(q, k, v, packed, out=None, lse=None, q_rope=None, k_rope=None, q_scale=None, k_scale=None,
-                  cu_seqlens_q=None, cu_seqlens_k=None):
+                  cu_seqlens_q=None, cu_seqlens_k=None, cu_seqlens_v=None):
     """Shapes (and, for the tensors passed as bare pointers, contiguity) that
     the library's sizes are derived from; a mismatch would make it read or
     write outside a tensor, so it is refused here."""
@@ -169,7 +170,13 @@ def _check_layout(q, k, v, packed, out=None, lse=None, q_rope=None, k_rope=None,
         b = shape(cu_seqlens_q)[0] - 1
         need(shape(cu_seqlens_k) == (b + 1,), "cu_seqlens_k must have the length of cu_seqlens_q")
         dv = shape(v)[1] if v_fp8 else shape(v)[-1]
-        need(shape(v) == ((hkv, dv, tk) if v_fp8 else (tk, hkv, dv)), f"v shape {shape(v)} does not match k")
+        if v_fp8:
+            # [Hkv, Dv, Tv]: sequence b at keys cu_seqlens_v[b] ... (checked on the device)
+            need(len(shape(v)) == 3 and shape(v)[0] == hkv, f"v shape {shape(v)} does not match k")
+            need(cu_seqlens_v is not None and shape(cu_seqlens_v) == (b + 1,),
+                 "packed e4m3 v needs cu_seqlens_v of the length of cu_seqlens_q")
+        else:
+            need(shape(v) == (tk, hkv, dv), f"v shape {shape(v)} does not match k")
         o_shape, lse_shape = (tq, hq, dv), (hq, tq)
         qs_shape, ks_shape, kr_lead = (hq, tq), (hkv, tk), (tk,)
     else:
@@ -193,18 +200,20 @@ def _check_layout(q, k, v, packed, out=None, lse=None, q_rope=None, k_rope=None,
         r = shape(q_rope)[-1]
         need(shape(q_rope) == shape(q)[:-1] + (r,), "q_rope must match q but for its depth")
         need(k_rope is not None and shape(k_rope) == kr_lead + (r,), f"k_rope must be {kr_lead + (r,)}")
-    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k), ("cu_seqlens_v", cu_seqlens_v)):
         if isinstance(t, torch.Tensor):
             need(t.is_contiguous() and t.dtype == torch.int32, f"{name} must be a contiguous int32 tensor")
 
 
 def make_params(q, k, v, *, causal, softmax_scale=None, q_rope=None, k_rope=None, q_scale=None, k_scale=None,
                 cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, out=None, lse=None,
-                workspace=None, backend="tcgen05", num_splits=0, schedule="dynamic", pair_cta="auto") -> Params:
+                workspace=None, backend="tcgen05", num_splits=0, schedule="dynamic", pair_cta="auto",
+                cu_seqlens_v=None) -> Params:
     """attn_fwd_params for torch tensors (shapes are read, nothing is allocated)."""
     packed = cu_seqlens_q is not None
     _check_layout(q, k, v, packed, out=out, lse=lse, q_rope=q_rope, k_rope=k_rope, q_scale=q_scale,
-                  k_scale=k_scale, cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k)
+                  k_scale=k_scale, cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k,
+                  cu_seqlens_v=cu_seqlens_v if v.dtype == torch.float8_e4m3fn else None)
     p = Params()
     if packed:
         tq, hq, d = q.shape
@@ -237,6 +246,8 @@ def make_params(q, k, v, *, causal, softmax_scale=None, q_rope=None, k_rope=None
     p.q_rope, p.k_rope = _ptr(q_rope), _ptr(k_rope)
     p.q_scale, p.k_scale = _ptr(q_scale), _ptr(k_scale)
     p.cu_seqlens_q, p.cu_seqlens_k = _ptr(cu_seqlens_q), _ptr(cu_seqlens_k)
+    if packed and v_fp8:
+        p.cu_seqlens_v, p.total_v = _ptr(cu_seqlens_v), v.shape[2]
     p.o = _ptr(out)
     p.lse = _ptr(lse)
     if workspace is not None:
@@ -265,13 +276,15 @@ def make_params(q, k, v, *, causal, softmax_scale=None, q_rope=None, k_rope=None
 def forward(q, k, v, *, causal=False, softmax_scale=None, q_rope=None, k_rope=None, q_scale=None, k_scale=None,
             cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, out=None, lse=None,
             return_lse=True, workspace=None, backend="tcgen05", stream=None, num_splits=0, schedule="dynamic",
-            pair_cta="auto"):
+            pair_cta="auto", cu_seqlens_v=None):
     """Fused attention forward on the GPU; returns (O, LSE).
 
     Fixed length: q [B,Sq,Hq,D], k [B,Sk,Hkv,D], v [B,Sk,Hkv,Dv] (e4m3 v:
     depth-major [B,Hkv,Dv,Sk], with e4m3 q/k; P is then rounded to e4m3) -> O
     [B,Sq,Hq,Dv] bf16, LSE [B,Hq,Sq] fp32. Packed: q [Tq,Hq,D] etc. with int32
-    cu_seqlens_q / cu_seqlens_k -> O [Tq,Hq,Dv], LSE [Hq,Tq]. Optional rope
+    cu_seqlens_q / cu_seqlens_k -> O [Tq,Hq,Dv], LSE [Hq,Tq]; packed e4m3 v is
+    [Hkv,Dv,Tv] with int32 cu_seqlens_v, each sequence's keys starting at a
+    multiple of 16. Optional rope
     parts q_rope [..,Hq,R] and k_rope [..,R] (one per token, shared by heads);
     fp8 e4m3 q/k need per-token fp32 scales q_scale [B,Hq,Sq] / [Hq,Tq] and
     k_scale [B,Hkv,Sk] / [Hkv,Tk]. ``num_splits``: split-KV key ranges per
@@ -283,7 +296,8 @@ def forward(q, k, v, *, causal=False, softmax_scale=None, q_rope=None, k_rope=No
     (default: the current torch stream).
     """
     for name, t in (("q", q), ("k", k), ("v", v), ("q_rope", q_rope), ("k_rope", k_rope), ("q_scale", q_scale),
-                    ("k_scale", k_scale), ("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+                    ("k_scale", k_scale), ("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k),
+                    ("cu_seqlens_v", cu_seqlens_v)):
         _require_cuda(name, t)
     L = lib()
     packed = cu_seqlens_q is not None
@@ -299,7 +313,7 @@ def forward(q, k, v, *, causal=False, softmax_scale=None, q_rope=None, k_rope=No
                     q_scale=q_scale, k_scale=k_scale, cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k,
                     max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k, out=out, lse=lse,
                     workspace=workspace, backend=backend, num_splits=num_splits, schedule=schedule,
-                    pair_cta=pair_cta)
+                    pair_cta=pair_cta, cu_seqlens_v=cu_seqlens_v)
     if workspace is None:
         with torch.cuda.device(dev):
             need = workspace_bytes(p)
@@ -333,7 +347,7 @@ class PreparedForward:
         if kw.get("lse") is None:
             shape = (q.shape[1], q.shape[0]) if packed else (q.shape[0], q.shape[2], q.shape[1])
             kw["lse"] = torch.empty(shape, dtype=torch.float32, device=dev)
-        for name in ("q_rope", "k_rope", "q_scale", "k_scale", "cu_seqlens_q", "cu_seqlens_k"):
+        for name in ("q_rope", "k_rope", "q_scale", "k_scale", "cu_seqlens_q", "cu_seqlens_k", "cu_seqlens_v"):
             _require_cuda(name, kw.get(name))
         self.out, self.lse = kw["out"], kw["lse"]
         self._keep = (q, k, v, kw)   # the tensors must outlive the prepared call

@@ -97,7 +97,9 @@ attn_status validate(const attn_fwd_params* p) {
   }
   if (p->v_dtype == ATTN_DTYPE_FP8_E4M3) {
     if (p->qk_dtype != ATTN_DTYPE_FP8_E4M3) return fail(ATTN_ERR_UNSUPPORTED, "fp8 V needs fp8 Q/K");
-    if (packed) return fail(ATTN_ERR_UNSUPPORTED, "fp8 V supports fixed-length sequences only");
+    if (packed && !no_keys && !no_queries &&
+        (p->cu_seqlens_v == nullptr || (reinterpret_cast<uintptr_t>(p->cu_seqlens_v) & 3) || p->total_v <= 0))
+      return fail(ATTN_ERR_INVALID_ARG, "packed fp8 V needs cu_seqlens_v (4-byte aligned) and total_v");
     if (p->head_dim_qk != 128 || p->head_dim_v != 128)
       return fail(ATTN_ERR_UNSUPPORTED, "fp8 V supports Dqk = Dv = 128 only");
     if (p->v_stride[1] % 16)
@@ -349,18 +351,22 @@ attn_status make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt,
   return ATTN_OK;
 }
 
-// Depth-major fp8 V, [B][Hkv][Dv][Sk] with the keys contiguous: 4-D map over
-// (key, depth, head, batch); box {128 keys, Dv rows, 1, 1}, 128-byte swizzle,
-// so one box is the K-major B operand of the P.V product.
+// Depth-major fp8 V, [B][Hkv][Dv][Sk] (packed: [Hkv][Dv][Tv]) with the keys
+// contiguous: 4-D map over (key, depth, head, batch); box {128 keys, Dv rows,
+// 1, 1}, 128-byte swizzle, so one box is the K-major B operand of the P.V
+// product.
 attn_status make_map_vt(CUtensorMap* map, const attn_fwd_params* p, const void* base) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
-  const int64_t sk = p->seqlen_k > 0 ? p->seqlen_k : 1;
+  const bool packed = p->cu_seqlens_q != nullptr;
+  const int64_t nb = packed ? 1 : p->batch;
+  const int64_t keys = packed ? p->total_v : p->seqlen_k;
+  const int64_t sk = keys > 0 ? keys : 1;
   const int64_t sd = p->v_stride[1];
   const int64_t sh = p->num_heads_kv > 1 ? p->v_stride[2] : sd * p->head_dim_v;
-  const int64_t sb = p->batch > 1 ? p->v_stride[0] : sh * p->num_heads_kv;
+  const int64_t sb = nb > 1 ? p->v_stride[0] : sh * p->num_heads_kv;
   cuuint64_t dims[4] = {(cuuint64_t)sk, (cuuint64_t)p->head_dim_v, (cuuint64_t)p->num_heads_kv,
-                        (cuuint64_t)p->batch};
+                        (cuuint64_t)nb};
   cuuint64_t strides[3] = {(cuuint64_t)sd, (cuuint64_t)sh, (cuuint64_t)sb};
   cuuint32_t box[4] = {(cuuint32_t)af::kBlockN, (cuuint32_t)p->head_dim_v, 1u, 1u};
   CUresult r = encode_4d_cached(fn, map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, dims, strides, box);
@@ -410,6 +416,8 @@ attn_status launch_tc05(const attn_fwd_params* p, cudaStream_t stream) {
   prm.k_scale = p->k_scale;
   prm.cu_q = p->cu_seqlens_q;
   prm.cu_k = p->cu_seqlens_k;
+  prm.cu_v = (packed && p->v_dtype == ATTN_DTYPE_FP8_E4M3) ? p->cu_seqlens_v : nullptr;
+  prm.total_v = prm.cu_v != nullptr ? p->total_v : 0;
   prm.o = static_cast<uint16_t*>(p->o);
   prm.lse = p->lse;
   prm.ws = static_cast<uint32_t*>(p->workspace);

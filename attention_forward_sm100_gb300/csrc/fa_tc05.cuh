@@ -190,6 +190,7 @@ struct Tc05Traits {
 // and lk already describe the tile's own key range.
 struct SchedSlot {
   int32_t valid, b, h, t, q_start, lq, k_start, lk, split;
+  int32_t v_start;   // first key of the tile's range along V's key dimension (packed e4m3 V: own offsets)
 };
 
 struct Ctx {
@@ -314,7 +315,7 @@ __device__ __forceinline__ SchedSlot read_slot(const Ctx& c, int slot, int off_s
   const volatile int32_t* p = reinterpret_cast<const volatile int32_t*>(c.smem + off_sched + kSlotBytes * slot);
   SchedSlot s;
   s.valid = p[0]; s.b = p[1]; s.h = p[2]; s.t = p[3];
-  s.q_start = p[4]; s.lq = p[5]; s.k_start = p[6]; s.lk = p[7]; s.split = p[8];
+  s.q_start = p[4]; s.lq = p[5]; s.k_start = p[6]; s.lk = p[7]; s.split = p[8]; s.v_start = p[9];
   return s;
 }
 
@@ -328,7 +329,7 @@ struct Cursor {
 __device__ __forceinline__ SchedSlot decode_work(const Tc05Params& P, int64_t w, Cursor& cur) {
   SchedSlot s;
   s.valid = 0;
-  s.b = s.h = s.t = s.q_start = s.k_start = s.split = 0;
+  s.b = s.h = s.t = s.q_start = s.k_start = s.split = s.v_start = 0;
   s.lq = P.seqlen_q;
   s.lk = P.seqlen_k;
   if (!P.packed) {
@@ -341,6 +342,7 @@ __device__ __forceinline__ SchedSlot decode_work(const Tc05Params& P, int64_t w,
         s.k_start = j0 * kBlockN;
         s.lk = min(P.seqlen_k, j1 * kBlockN) - s.k_start;
       }
+      s.v_start = s.k_start;
     }
     return s;
   }
@@ -355,6 +357,11 @@ __device__ __forceinline__ SchedSlot decode_work(const Tc05Params& P, int64_t w,
       // one whose work index runs past the batch scans to its end).
       const int qs = P.cu_q[bb], qe = P.cu_q[bb + 1], ks = P.cu_k[bb], ke = P.cu_k[bb + 1];
       bad = qs < 0 || qe < qs || qe > P.total_q || ks < 0 || ke < ks || ke > P.total_k;
+      if (P.cu_v != nullptr) {
+        // packed e4m3 V: each sequence's keys start on a 16-key boundary of V
+        const int vs = P.cu_v[bb];
+        bad = bad || vs < 0 || (vs & 15) != 0 || (int64_t)vs + (ke - ks) > (int64_t)P.total_v;
+      }
       if (!bad) u = (int64_t)tiles_for(qe - qs, P.rows_per_tile) * P.heads_q * P.num_splits;
     }
     const unsigned bad_lanes = __ballot_sync(kFull, bad);
@@ -391,6 +398,7 @@ __device__ __forceinline__ SchedSlot decode_work(const Tc05Params& P, int64_t w,
         s.k_start = ks + j0 * kBlockN;
         s.lk = min(ke - ks, j1 * kBlockN) - j0 * kBlockN;
       }
+      s.v_start = P.cu_v != nullptr ? P.cu_v[b] + (s.k_start - ks) : s.k_start;
       return s;
     }
     if (cur.b + 32 >= P.batch) return s;
@@ -443,7 +451,7 @@ __device__ void role_load_qk(const Tc05Params& P, const Ctx& c) {
     if (lane == 0) {
       volatile int32_t* p = reinterpret_cast<volatile int32_t*>(c.smem + T::OFF_SCHED + kSlotBytes * sched.idx);
       p[0] = s.valid; p[1] = s.b; p[2] = s.h; p[3] = s.t;
-      p[4] = s.q_start; p[5] = s.lq; p[6] = s.k_start; p[7] = s.lk; p[8] = s.split;
+      p[4] = s.q_start; p[5] = s.lq; p[6] = s.k_start; p[7] = s.lk; p[8] = s.split; p[9] = s.v_start;
       ptx::mbar_arrive(c.bar(BAR_SCHED_FULL + sched.idx));
     }
     __syncwarp();
@@ -580,8 +588,9 @@ __device__ void role_load_v(const Tc05Params& P, const Ctx& c) {
         if (lead) ptx::mbar_expect_tx(bar, T::V_TX);
         if (T::V8) {
           // depth-major e4m3 V: coordinates (key, depth row, head, batch); the
-          // key coordinate is a multiple of 128 (fixed-length sequences only)
-          ptx::tma_load_4d(dst, &P.tm_v, bar, row, 0, hk, vb);
+          // key coordinate is a multiple of 16 (a multiple of 128 for fixed
+          // length; packed sequences start on 16-key boundaries of V)
+          ptx::tma_load_4d(dst, &P.tm_v, bar, s.v_start + kBlockN * j, 0, hk, vb);
         } else if (T::PAIR) {
           // a pair's CTA r holds depth columns [64 r, 64 r + 64) of the tile
           load_box<T>(c, dst, &P.tm_v, bar, 64 * (int)c.rank, hk, row, vb);

@@ -43,6 +43,8 @@ struct Tc05Params {
   const float* k_scale;
   const int32_t* cu_q;     // packed only
   const int32_t* cu_k;
+  const int32_t* cu_v;     // packed e4m3 V only: key starts of the sequences along V's key dimension
+  int32_t total_v;         // packed e4m3 V: length of V's key dimension
   uint16_t* o;             // output rows (bf16 bits)
   float* lse;
   uint32_t* ws;            // workspace words

@@ -15,7 +15,9 @@ Recipe (the reading taken for every workload):
     the quantised value is clamp(x / scale, -448, 448) rounded to e4m3;
   * all-FP8 workloads also round V (drawn after K, N(0,1)) to e4m3 without a
     scale (clamp to +-448, nearest even) and store it depth-major, each row
-    of keys padded with zeros to a multiple of 16.
+    of keys padded with zeros to a multiple of 16; packed: [Hkv, Dv, Tv] with
+    every sequence's keys starting at a multiple of 16 (int32 cu_seqlens_v
+    gives those starts, zeros between sequences).
 
 Layouts: Q/K/V/O are [B, S, H, D] (fixed length) or [T, H, D] (packed, with
 int32 cu_seqlens of length B + 1). The shared K rope part is [B, S, R] or
@@ -47,7 +49,7 @@ class AttnSpec:
     seed: int
     rope: int = 0            # rope depth R (K rope shared by all heads)
     qk_dtype: str = "bf16"   # "bf16" or "fp8"
-    v_dtype: str = "bf16"    # "bf16", or "fp8": e4m3 V stored depth-major [B, Hkv, Dv, Sk]
+    v_dtype: str = "bf16"    # "bf16", or "fp8": e4m3 V depth-major [B, Hkv, Dv, Sk] (packed: [Hkv, Dv, Tv])
     lengths_q: Optional[Sequence[int]] = None   # packed layout when set
     lengths_k: Optional[Sequence[int]] = None   # defaults to lengths_q
     scale: Optional[float] = None               # defaults to 1/sqrt(d_qk + rope)
@@ -180,11 +182,20 @@ def _scales_token_contiguous(scale: torch.Tensor, varlen: bool) -> torch.Tensor:
     return scale.permute(0, 2, 1).contiguous()
 
 
-def v_token_major(v: torch.Tensor) -> torch.Tensor:
-    """V as [B, Sk, Hkv, Dv] (a view): depth-major e4m3 V is permuted back."""
-    if v.dtype == torch.float8_e4m3fn:
+def v_token_major(v: torch.Tensor, cu_seqlens_k=None, cu_seqlens_v=None) -> torch.Tensor:
+    """V as [B, Sk, Hkv, Dv] (fixed length: a view) or [Tk, Hkv, Dv] (packed):
+    depth-major e4m3 V is permuted back, and packed e4m3 V ([Hkv, Dv, Tv],
+    sequence b at keys cu_seqlens_v[b] ...) is gathered into token order."""
+    if v.dtype != torch.float8_e4m3fn:
+        return v
+    if v.dim() == 4:
         return v.permute(0, 3, 1, 2)
-    return v
+    parts = []
+    for b in range(len(cu_seqlens_k) - 1):
+        n = int(cu_seqlens_k[b + 1]) - int(cu_seqlens_k[b])
+        s = int(cu_seqlens_v[b])
+        parts.append(v[:, :, s:s + n].permute(2, 0, 1))
+    return torch.cat(parts, dim=0)
 
 
 def to_device(inputs: dict, device) -> dict:
@@ -243,9 +254,21 @@ def make_inputs(spec: AttnSpec) -> dict:
         q32 = randn(*qshape, spec.d_qk)
         k32 = randn(*kshape, spec.d_qk)
         v32 = randn(*kshape, spec.d_v)
-        if spec.v_dtype == "fp8":
-            if spec.varlen:
-                raise ValueError("e4m3 V is defined for fixed-length workloads only")
+        if spec.v_dtype == "fp8" and spec.varlen:
+            v8 = torch.clamp(v32, -FP8_E4M3_MAX, FP8_E4M3_MAX).to(torch.float8_e4m3fn)
+            # [Tk, Hkv, Dv] -> [Hkv, Dv, Tv]: each sequence's keys start at a
+            # multiple of 16 keys (16 bytes, the alignment of a TMA
+            # coordinate along the contiguous dimension)
+            cv = [0]
+            for n in lk:
+                cv.append(cv[-1] + (n + 15) // 16 * 16)
+            vt = torch.zeros((spec.heads_kv, spec.d_v, max(cv[-1], 16)), dtype=torch.float8_e4m3fn)
+            ck = out["cu_seqlens_k"].tolist()
+            for b in range(len(lk)):
+                vt[:, :, cv[b]:cv[b] + lk[b]] = v8[ck[b]:ck[b + 1]].permute(1, 2, 0)
+            v = vt
+            out["cu_seqlens_v"] = torch.tensor(cv, dtype=torch.int32)
+        elif spec.v_dtype == "fp8":
             v8 = torch.clamp(v32, -FP8_E4M3_MAX, FP8_E4M3_MAX).to(torch.float8_e4m3fn)
             # [B, Sk, Hkv, Dv] -> [B, Hkv, Dv, Sk]; the rows of keys are padded
             # to a multiple of 16 bytes (the alignment a TMA row stride needs)

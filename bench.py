@@ -170,7 +170,8 @@ def cpu_baseline(spec, inputs, seconds):
     cores = len(os.sched_getaffinity(0))
     lq, lk = spec.seq_lengths()
     from attention_forward_sm100_gb300.workloads import v_token_major
-    q, k, v = f64(inputs["q"]), f64(inputs["k"]), f64(v_token_major(inputs["v"]))
+    q, k = f64(inputs["q"]), f64(inputs["k"])
+    v = f64(v_token_major(inputs["v"], inputs.get("cu_seqlens_k"), inputs.get("cu_seqlens_v")))
     qr, kr = f64(inputs.get("q_rope")), f64(inputs.get("k_rope"))
     qs, ks = f64(inputs.get("q_scale")), f64(inputs.get("k_scale"))
     cu_q = inputs.get("cu_seqlens_q")
@@ -293,7 +294,7 @@ def prepare(spec, dev, schedule):
     kw = dict(causal=spec.causal, softmax_scale=spec.softmax_scale, q_rope=d.get("q_rope"), k_rope=d.get("k_rope"),
               q_scale=d.get("q_scale"), k_scale=d.get("k_scale"), cu_seqlens_q=d.get("cu_seqlens_q"),
               cu_seqlens_k=d.get("cu_seqlens_k"), max_seqlen_q=max(lq), max_seqlen_k=max(lk), out=out, lse=lse,
-              schedule=schedule)
+              schedule=schedule, cu_seqlens_v=d.get("cu_seqlens_v"))
     prm = pkg.make_params(d["q"], d["k"], d["v"], **kw)
     ws = pkg.default_workspace(dev, pkg.workspace_bytes(prm))
     prm.workspace, prm.workspace_bytes = ws.data_ptr(), ws.numel()
@@ -522,7 +523,8 @@ def main():
         # would run them: two device buffer sets, the upload of step k+1 on
         # its own stream while step k computes and step k-1 downloads; the
         # timed region runs from the first upload to the last download.
-        names = ("q", "k", "v", "q_rope", "k_rope", "q_scale", "k_scale", "cu_seqlens_q", "cu_seqlens_k")
+        names = ("q", "k", "v", "q_rope", "k_rope", "q_scale", "k_scale", "cu_seqlens_q", "cu_seqlens_k",
+                 "cu_seqlens_v")
         hin = {n: inputs[n].pin_memory() for n in names if inputs.get(n) is not None}
         h2d = sum(t.numel() * t.element_size() for t in hin.values())
         slots = []
@@ -551,7 +553,8 @@ def main():
             di = sl["din"]
             pkg.forward(di["q"], di["k"], di["v"], q_rope=di.get("q_rope"), k_rope=di.get("k_rope"),
                         q_scale=di.get("q_scale"), k_scale=di.get("k_scale"), cu_seqlens_q=di.get("cu_seqlens_q"),
-                        cu_seqlens_k=di.get("cu_seqlens_k"), out=sl["o"], lse=sl["lse"], stream=stream, **kw_e)
+                        cu_seqlens_k=di.get("cu_seqlens_k"), cu_seqlens_v=di.get("cu_seqlens_v"), out=sl["o"],
+                        lse=sl["lse"], stream=stream, **kw_e)
             sl["computed"].record(stream)
             down.wait_event(sl["computed"])
             with torch.cuda.stream(down):

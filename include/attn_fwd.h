@@ -104,8 +104,9 @@ typedef struct attn_fwd_params {
   const void *q;        /* fixed [B,Sq,Hq,Dqk] / packed [Tq,Hq,Dqk]; bf16 or fp8 (qk_dtype) */
   const void *k;        /* fixed [B,Sk,Hkv,Dqk] / packed [Tk,Hkv,Dqk]; same type as q */
   const void *v;        /* bf16 (v_dtype BF16): fixed [B,Sk,Hkv,Dv] / packed [Tk,Hkv,Dv];
-                           fp8 e4m3 (v_dtype FP8_E4M3, fixed length only): depth-major
-                           [B,Hkv,Dv,Sk] with the keys contiguous (v_stride: see below) */
+                           fp8 e4m3 (v_dtype FP8_E4M3): depth-major with the keys contiguous,
+                           fixed [B,Hkv,Dv,Sk] / packed [Hkv,Dv,Tv] (sequence b at keys
+                           cu_seqlens_v[b] ...; v_stride: see below) */
   const void *q_rope;   /* rope_depth > 0 only: [B,Sq,Hq,R] / [Tq,Hq,R]; bf16 */
   const void *k_rope;   /* rope_depth > 0 only: [B,Sk,R] / [Tk,R]; bf16, shared by all heads */
   const float *q_scale; /* fp8 only: [B,Hq,Sq] / [Hq,Tq], contiguous fp32 */
@@ -134,7 +135,7 @@ typedef struct attn_fwd_params {
   float softmax_scale;  /* scale of the scores; > 0 */
   int32_t qk_dtype;     /* attn_dtype */
   int32_t v_dtype;      /* attn_dtype of v: BF16, or FP8_E4M3 (needs fp8 q/k, Dqk = Dv = 128,
-                           no rope, fixed length; no scale: V's e4m3 values are used as is) */
+                           no rope; no scale: V's e4m3 values are used as is) */
   int32_t backend;      /* attn_backend */
 
   /* ---- element strides: [0] batch (unused when packed), [1] token, [2] head.
@@ -170,6 +171,14 @@ typedef struct attn_fwd_params {
   /* attn_pair_cta. ATTN_PAIR_ON outside its supported configurations (see
    * attn_pair_cta) is UNSUPPORTED; with it fault_injection must be 0. */
   int32_t pair_cta;
+
+  /* Packed e4m3 V only (NULL otherwise): [B+1] device int32, the key index
+   * along V's contiguous key dimension where sequence b's Lk_b keys start;
+   * every start must be a multiple of 16 (a TMA copy starts on a 16-byte
+   * boundary) and start + Lk_b <= total_v. The kernel checks this and
+   * reports a violation through attn_fwd_check as INVALID_ARG. */
+  const int32_t *cu_seqlens_v;
+  int32_t total_v;          /* packed e4m3 V: Tv, the length of V's key dimension */
 } attn_fwd_params;
 
 /* Query results of attn_fwd_plan (host only; no GPU needed). */

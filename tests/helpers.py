@@ -25,9 +25,9 @@ def oracle_args(inputs):
 
 
 def v_for_oracle(inputs):
-    """V in the oracle's [B, Sk, Hkv, Dv] layout, exact float64."""
+    """V in the oracle's [B, Sk, Hkv, Dv] (or packed [Tk, Hkv, Dv]) layout, exact float64."""
     from attention_forward_sm100_gb300.workloads import v_token_major
-    return f64(v_token_major(inputs["v"]))
+    return f64(v_token_major(inputs["v"], inputs.get("cu_seqlens_k"), inputs.get("cu_seqlens_v")))
 
 
 def run_oracle(inputs):
@@ -87,7 +87,7 @@ def run_lib(inputs, backend="tcgen05", device="cuda", num_splits=0, **kw):
     o, lse = pkg.forward(d["q"], d["k"], d["v"], causal=spec.causal, softmax_scale=spec.softmax_scale,
                          q_rope=d.get("q_rope"), k_rope=d.get("k_rope"), q_scale=d.get("q_scale"),
                          k_scale=d.get("k_scale"), cu_seqlens_q=d.get("cu_seqlens_q"),
-                         cu_seqlens_k=d.get("cu_seqlens_k"), max_seqlen_q=max(lq + [0]),
+                         cu_seqlens_k=d.get("cu_seqlens_k"), cu_seqlens_v=d.get("cu_seqlens_v"), max_seqlen_q=max(lq + [0]),
                          max_seqlen_k=max(lk + [0]), backend=backend, num_splits=num_splits, **kw)
     pkg.check(device=dev)
     return o.cpu(), lse.cpu()

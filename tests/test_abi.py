@@ -281,7 +281,7 @@ def test_schedule_mode_rejected(pkg):
 
 
 # ---------------------------------------------------------------- all-FP8
-@pytest.mark.parametrize("case,status", [("bf16_qk", 2), ("packed", 2), ("dv64", 2), ("row_stride", 1)])
+@pytest.mark.parametrize("case,status", [("bf16_qk", 2), ("packed_no_cu_v", 1), ("dv64", 2), ("row_stride", 1)])
 def test_fp8_v_rejections(pkg, case, status):
     f8 = torch.float8_e4m3fn
     qdt = torch.bfloat16 if case == "bf16_qk" else f8
@@ -295,16 +295,21 @@ def test_fp8_v_rejections(pkg, case, status):
     ksc = _Fake((1, 4, sk), dtype=torch.float32, ptr=9 << 20)
     ws = _Fake((256,), dtype=torch.uint8, ptr=5 << 20)
     kw = {}
-    if case == "packed":
+    if case == "packed_no_cu_v":
         q = _Fake((256, 4, 128), dtype=f8, ptr=1 << 20)
         k = _Fake((sk, 4, 128), dtype=f8, ptr=2 << 20)
         v = _Fake((4, dv, sk), dtype=f8, ptr=3 << 20)
         o = _Fake((256, 4, dv), ptr=4 << 20)
         qsc = _Fake((4, 256), dtype=torch.float32, ptr=6 << 20)
         ksc = _Fake((4, sk), dtype=torch.float32, ptr=9 << 20)
-        kw = dict(cu_seqlens_q=_Fake((2,), ptr=7 << 20), cu_seqlens_k=_Fake((2,), ptr=8 << 20))
+        kw = dict(cu_seqlens_q=_Fake((2,), ptr=7 << 20), cu_seqlens_k=_Fake((2,), ptr=8 << 20),
+                  cu_seqlens_v=_Fake((2,), ptr=10 << 20))
     p = pkg.make_params(q, k, v, causal=True, out=o, lse=None, workspace=ws, q_scale=qsc, k_scale=ksc, **kw)
     assert p.v_dtype == 1 and p.head_dim_v == dv
+    if case == "packed_no_cu_v":
+        pkg.plan(p)                       # accepted with the key offsets of V ...
+        p.cu_seqlens_v = None             # ... refused without them
+        assert p.total_v == sk
     with pytest.raises(pkg.AttnError) as e:
         pkg.plan(p)
     assert e.value.status == status

@@ -36,6 +36,12 @@ CASES = {
     "noncausal_sk1": (_fp8qkv(1, 2, 2, 130, 16, 128, 128, False, seed=113), 1),
     "noncausal_split3": (_fp8qkv(1, 4, 2, 256, 2048, 128, 128, False, seed=114), 3),
     "causal_sq300_sk160": (_fp8qkv(1, 2, 2, 300, 160, 128, 128, True, seed=115), 1),
+    # packed sequences: V's keys per sequence start on 16-key boundaries
+    "packed_causal_gqa": (_fp8qkv(4, 8, 2, 640, 640, 128, 128, True, seed=117, lengths_q=(1, 300, 129, 640)), 1),
+    "packed_noncausal_qk_differ": (_fp8qkv(3, 4, 4, 400, 400, 128, 128, False, seed=118, lengths_q=(257, 3, 130),
+                                           lengths_k=(5, 400, 131)), 1),
+    "packed_noncausal_split3": (_fp8qkv(2, 4, 2, 200, 1500, 128, 128, False, seed=119, lengths_q=(200, 77),
+                                        lengths_k=(1500, 333)), 3),
 }
 
 
@@ -45,14 +51,24 @@ def _bound_rows(inp, rows):
     args = oracle_args(inp)
     q, k, v = f64(inp["q"]), f64(inp["k"]), v_for_oracle(inp)
     g = spec.heads_q // spec.heads_kv
+    lq, lk = spec.seq_lengths()
     out = []
     for b, h, i in rows:
         hk = h // g
-        s = oracle.scores(q[b, i:i + 1, h], k[b, :, hk], args["scale"],
-                          qs=args["q_scale"][b, h, i:i + 1], ks=args["k_scale"][b, hk])
-        vis = oracle.visible_mask(spec.seqlen_q, spec.seqlen_k, spec.causal, rows=[i])
+        if spec.varlen:
+            a, c = int(args["cu_seqlens_q"][b]), int(args["cu_seqlens_k"][b])
+            qr, kr, vr = q[a + i:a + i + 1, h], k[c:c + lk[b], hk], v[c:c + lk[b], hk]
+            qs, ks = args["q_scale"][h, a + i:a + i + 1], args["k_scale"][hk, c:c + lk[b]]
+        else:
+            qr, kr, vr = q[b, i:i + 1, h], k[b, :, hk], v[b, :, hk]
+            qs, ks = args["q_scale"][b, h, i:i + 1], args["k_scale"][b, hk]
+        s = oracle.scores(qr, kr, args["scale"], qs=qs, ks=ks)
+        vis = oracle.visible_mask(lq[b], lk[b], spec.causal, rows=[i])
+        if not vis.any():
+            out.append(np.zeros(vr.shape[-1]))
+            continue
         w, lse = oracle.softmax_lse(s, vis)
-        av = np.abs(v[b, :, hk])
+        av = np.abs(vr)
         smax = np.where(vis, s, -np.inf).max()
         out.append(2.0 ** -4 * (w @ av)[0] + 2.0 ** -10 * np.exp(smax - lse[0]) * (vis[0] @ av))
     return np.array(out)
@@ -62,7 +78,7 @@ def _check(inp, o, lse, rows):
     spec = inp["spec"]
     o_ref, l_ref = oracle.attention_rows(f64(inp["q"]), f64(inp["k"]), v_for_oracle(inp), rows,
                                          **oracle_args(inp))
-    o_gpu, l_gpu = gather_rows(spec, o, lse, rows)
+    o_gpu, l_gpu = gather_rows(spec, o, lse, rows, inp.get("cu_seqlens_q"))
     bound = _bound_rows(inp, rows) + 2.0 ** -8 * np.abs(o_ref) + 1e-4
     err = np.abs(o_gpu - o_ref)
     worst = float((err / bound).max())
@@ -75,7 +91,8 @@ def _check(inp, o, lse, rows):
 
 
 def _all_rows(spec):
-    return [(b, h, i) for b in range(spec.batch) for h in range(spec.heads_q) for i in range(spec.seqlen_q)]
+    lq, _ = spec.seq_lengths()
+    return [(b, h, i) for b in range(spec.batch) for h in range(spec.heads_q) for i in range(lq[b])]
 
 
 @pytest.mark.gpu

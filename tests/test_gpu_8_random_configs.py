@@ -18,7 +18,7 @@ def _draw_case(seed):
     rng = np.random.default_rng(1000 + seed)
     kind = rng.choice(["d64", "d128", "rope", "fp8", "fp8qkv"])
     causal = bool(rng.integers(2))
-    packed = kind != "fp8qkv" and bool(rng.integers(2))
+    packed = bool(rng.integers(2))
     b = int(rng.integers(1, 4))
     hkv = int(rng.choice([1, 2, 4]))
     hq = hkv * int(rng.choice([1, 2, 4]))
@@ -53,8 +53,8 @@ def test_random_config(seed):
     o, lse = pkg.forward(d["q"], d["k"], d["v"], causal=spec.causal, softmax_scale=spec.softmax_scale,
                          q_rope=d.get("q_rope"), k_rope=d.get("k_rope"), q_scale=d.get("q_scale"),
                          k_scale=d.get("k_scale"), cu_seqlens_q=d.get("cu_seqlens_q"),
-                         cu_seqlens_k=d.get("cu_seqlens_k"), max_seqlen_q=max(lq), max_seqlen_k=max(lk),
-                         num_splits=splits, schedule=schedule)
+                         cu_seqlens_k=d.get("cu_seqlens_k"), cu_seqlens_v=d.get("cu_seqlens_v"),
+                         max_seqlen_q=max(lq), max_seqlen_k=max(lk), num_splits=splits, schedule=schedule)
     pkg.check(device=dev)
     o_ref, lse_ref = run_oracle(inp)
     err = errors(f64(o.cpu()), o_ref, lse.cpu().double().numpy(), lse_ref)

@@ -127,3 +127,23 @@ def test_tile_granular_flops():
     assert 1.03 < spec.flops_tile_granular() / spec.flops() < 1.032
     nc = W.WORKLOADS["mha_b1_h2_s128_d64_noncausal"]
     assert nc.flops_tile_granular() == nc.flops()
+
+
+def test_packed_e4m3_v_layout():
+    """Packed e4m3 V: [Hkv, Dv, Tv], each sequence's keys at a multiple of 16
+    (zeros between sequences), and the gather back to token order returns
+    exactly the rounded draws."""
+    import torch
+    spec = W.AttnSpec(3, 4, 2, 300, 300, 128, 128, True, seed=9, qk_dtype="fp8", v_dtype="fp8",
+                      lengths_q=(17, 300, 1))
+    inp = W.make_inputs(spec)
+    cv = inp["cu_seqlens_v"].tolist()
+    assert cv == [0, 32, 336, 352]
+    assert all(c % 16 == 0 for c in cv)
+    v = inp["v"]
+    assert tuple(v.shape) == (2, 128, 352)
+    tm = W.v_token_major(v, inp["cu_seqlens_k"], inp["cu_seqlens_v"])
+    assert tuple(tm.shape) == (318, 2, 128)
+    # zeros between sequences; the gather reads each sequence's own keys
+    assert torch.equal(v[:, :, 17:32].float(), torch.zeros(2, 128, 15))
+    assert torch.equal(tm[:17].float(), v[:, :, 0:17].permute(2, 0, 1).float())
