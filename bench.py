@@ -6,7 +6,7 @@ the workload splits) over the chosen workload, inputs resident in HBM.
 Prints one JSON line on rank 0.
 
   python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl ours|reference]
-                  [--schedule dynamic|static|grid] [--no-workloads]
+                  [--schedule dynamic|static|grid] [--pair-cta auto|off|on] [--no-workloads]
 
 After the headline workload (its JSON keys: value, roofline, e2e, clocks,
 cpu_baseline), a one-GPU run also times every other workload the same way
@@ -80,6 +80,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--pair-cta", default="auto", choices=["auto", "off", "on"],
+                    help="CTA pairs for the headline workload")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip timing the other task workloads after the headline one")
     return ap.parse_args()
@@ -475,6 +477,7 @@ def main():
     # Kernels per call: the attention kernel, plus the merge kernel when the
     # library splits the keys of each query tile (split-KV).
     inputs, d, kw, out, lse, num_splits, launches_per_step = prepare(spec, dev, args.schedule)
+    kw["pair_cta"] = args.pair_cta
     in_bytes = sum(t.numel() * t.element_size() for t in d.values() if isinstance(t, torch.Tensor))
 
     def step():
@@ -600,6 +603,7 @@ def main():
                        "heads_kv": spec.heads_kv, "seqlen": spec.seqlen_q, "head_dim_qk": spec.d_qk + spec.rope,
                        "head_dim_v": spec.d_v, "causal": spec.causal, "flops_per_step": flops,
                        "seqlen_k": spec.seqlen_k, "num_splits": num_splits, "schedule": args.schedule,
+                       "pair_cta": args.pair_cta,
                        "flops_tile_granular": spec.flops_tile_granular(),
                        "hbm_bytes_algorithmic": spec.hbm_bytes(),
                        "l2": "inputs larger than L2" if in_bytes > L2_BYTES else "inputs fit in L2 (no flush)",
@@ -608,7 +612,7 @@ def main():
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak,
                          "peak_source": peak_label(spec, peak_src),
-                         "traffic": profiled_traffic(args.workload)},
+                         "traffic": profiled_traffic(args.workload) if args.pair_cta != "on" else None},
             "kernel_ms": kernel_ms,
             "median_ms": median_ms,
             "clocks": clk,
