@@ -877,13 +877,21 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
       const bool need_mask = (kb + kBlockN > s.lk) || (CAUSAL && kb + kBlockN - 1 > first_row);
       if (need_mask) {
         const int vis = lim - kb;
+        if constexpr (T::V8) {
+          // one compare per key (measured 5 % faster here than the per-chunk
+          // bit pattern below, which is ~1 % faster in the other variants)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int vq = min(max(vis - 32 * q, 0), 32);
-          const uint32_t bits = vq >= 32 ? 0xffffffffu : ((1u << vq) - 1u);
+          for (int e = 0; e < 128; ++e)
+            if (e >= vis) sv[e] = -INFINITY;
+        } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (!((bits >> e) & 1u)) sv[32 * q + e] = -INFINITY;
+          for (int q = 0; q < 4; ++q) {
+            const int vq = min(max(vis - 32 * q, 0), 32);
+            const uint32_t bits = vq >= 32 ? 0xffffffffu : ((1u << vq) - 1u);
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (!((bits >> e) & 1u)) sv[32 * q + e] = -INFINITY;
+          }
         }
       }
       float mx0 = ptx::max3(sv[0], sv[1], sv[2]), mx1 = ptx::max3(sv[3], sv[4], sv[5]);
