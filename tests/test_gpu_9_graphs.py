@@ -2,7 +2,8 @@
 travel by value in the launch parameters, the workspace counters are reset
 by the kernel itself), so a captured forward can be replayed with new data
 in the same input buffers. Every replay must equal, bit for bit, an eager
-call on the same data; a split-KV call captures both of its kernels."""
+call on the same data; a split-KV call captures both of its kernels, and a
+CTA-pair call its cluster launch."""
 import dataclasses
 
 import pytest
@@ -11,10 +12,13 @@ import torch
 from attention_forward_sm100_gb300 import workloads as W
 
 CASES = {
-    "bf16_causal_gqa": (W.AttnSpec(2, 8, 2, 700, 700, 128, 128, True, seed=130), 1),
-    "split_kv": (W.AttnSpec(1, 4, 2, 256, 3000, 128, 128, False, seed=131), 4),
-    "fp8qkv": (W.AttnSpec(1, 4, 4, 400, 400, 128, 128, True, seed=132, qk_dtype="fp8", v_dtype="fp8"), 1),
-    "d64_small": (W.AttnSpec(1, 2, 2, 128, 128, 64, 64, False, seed=133), 1),
+    # name: (spec, num_splits, extra options)
+    "bf16_causal_gqa": (W.AttnSpec(2, 8, 2, 700, 700, 128, 128, True, seed=130), 1, {}),
+    "split_kv": (W.AttnSpec(1, 4, 2, 256, 3000, 128, 128, False, seed=131), 4, {}),
+    "fp8qkv": (W.AttnSpec(1, 4, 4, 400, 400, 128, 128, True, seed=132, qk_dtype="fp8", v_dtype="fp8"), 1, {}),
+    "d64_small": (W.AttnSpec(1, 2, 2, 128, 128, 64, 64, False, seed=133), 1, {}),
+    "pairs_causal_gqa": (W.AttnSpec(2, 8, 2, 1100, 1100, 128, 128, True, seed=134), 1, {"pair_cta": "on"}),
+    "pairs_rope": (W.AttnSpec(1, 4, 4, 600, 600, 128, 128, True, seed=135, rope=64), 1, {"pair_cta": "on"}),
 }
 
 
@@ -22,11 +26,12 @@ CASES = {
 @pytest.mark.parametrize("name", sorted(CASES))
 def test_graph_replay_matches_eager(name):
     import attention_forward_sm100_gb300 as pkg
-    spec, splits = CASES[name]
+    spec, splits, extra = CASES[name]
     dev = torch.device("cuda")
     d = W.to_device(W.make_inputs(spec), dev)
     kw = dict(causal=spec.causal, softmax_scale=spec.softmax_scale, q_scale=d.get("q_scale"),
-              k_scale=d.get("k_scale"), num_splits=splits)
+              k_scale=d.get("k_scale"), q_rope=d.get("q_rope"), k_rope=d.get("k_rope"), num_splits=splits,
+              **extra)
     o = torch.empty(d["q"].shape[:-1] + (spec.d_v,), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((spec.batch, spec.heads_q, spec.seqlen_q), dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(dev)
@@ -38,7 +43,7 @@ def test_graph_replay_matches_eager(name):
         pkg.forward(d["q"], d["k"], d["v"], out=o, lse=lse, **kw)
     for rep in range(3):
         fresh = W.to_device(W.make_inputs(dataclasses.replace(spec, seed=spec.seed + 10 * (rep + 1))), dev)
-        for n in ("q", "k", "v", "q_scale", "k_scale"):
+        for n in ("q", "k", "v", "q_scale", "k_scale", "q_rope", "k_rope"):
             if d.get(n) is not None:
                 d[n].copy_(fresh[n])
         graph.replay()
@@ -47,3 +52,27 @@ def test_graph_replay_matches_eager(name):
         pkg.check(device=dev)
         assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16)), rep
         assert torch.equal(lse.view(torch.int32), l_ref.view(torch.int32)), rep
+
+
+@pytest.mark.gpu
+def test_prepared_call_matches_forward():
+    """prepare(...) marshals the arguments once; each run() must give what a
+    forward() call on the same buffers gives, also after the inputs change."""
+    import attention_forward_sm100_gb300 as pkg
+    spec = W.AttnSpec(2, 8, 2, 600, 600, 128, 128, True, seed=136, lengths_q=(600, 129))
+    dev = torch.device("cuda")
+    d = W.to_device(W.make_inputs(spec), dev)
+    lq, lk = spec.seq_lengths()
+    kw = dict(causal=True, softmax_scale=spec.softmax_scale, cu_seqlens_q=d["cu_seqlens_q"],
+              cu_seqlens_k=d["cu_seqlens_k"], max_seqlen_q=max(lq), max_seqlen_k=max(lk))
+    prep = pkg.prepare(d["q"], d["k"], d["v"], **kw)
+    for rep in range(3):
+        if rep:
+            fresh = W.to_device(W.make_inputs(dataclasses.replace(spec, seed=spec.seed + rep)), dev)
+            for n in ("q", "k", "v"):
+                d[n].copy_(fresh[n])
+        o, lse = prep.run()
+        o_ref, l_ref = pkg.forward(d["q"], d["k"], d["v"], **kw)
+        pkg.check(device=dev)
+        assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16)), rep
+        assert torch.equal(lse, l_ref), rep
