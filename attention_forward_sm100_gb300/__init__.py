@@ -7,8 +7,8 @@ small merge kernel); ``prepare`` fixes the tensors and options of a call so
 that repeated calls skip the argument marshalling. Build the library with
 ``attention_forward_sm100_gb300.build.build()``.
 """
-from ._binding import (AttnError, Params, PlanInfo, PreparedForward, check, default_workspace, forward, last_error,
-                       lib, make_params, plan, prepare, schedule, workspace_bytes)
+from ._binding import (AttnError, Params, PlanInfo, PreparedForward, check, default_workspace, forward, key_range,
+                       last_error, lib, make_params, plan, prepare, schedule, workspace_bytes)
 
 __all__ = ["AttnError", "Params", "PlanInfo", "PreparedForward", "check", "default_workspace", "forward",
-           "last_error", "lib", "make_params", "plan", "prepare", "schedule", "workspace_bytes"]
+           "key_range", "last_error", "lib", "make_params", "plan", "prepare", "schedule", "workspace_bytes"]

@@ -90,6 +90,10 @@ def lib():
             L.attn_fwd_schedule.argtypes = [ctypes.POINTER(Params), ctypes.c_void_p, ctypes.POINTER(WorkTile),
                                             ctypes.c_int64]
             L.attn_fwd_schedule.restype = ctypes.c_int64
+            L.attn_fwd_key_range.argtypes = [ctypes.POINTER(Params), ctypes.c_int32, ctypes.c_int32,
+                                             ctypes.c_int32, ctypes.POINTER(ctypes.c_int32),
+                                             ctypes.POINTER(ctypes.c_int32)]
+            L.attn_fwd_key_range.restype = ctypes.c_int
             L.attn_fwd_workspace_bytes.argtypes = [ctypes.POINTER(Params)]
             L.attn_fwd_workspace_bytes.restype = ctypes.c_size_t
             L.attn_fwd_params_init.argtypes = [ctypes.POINTER(Params)]
@@ -416,3 +420,14 @@ def schedule(p: Params, host_cu_seqlens_q=None, with_split=False):
     if with_split:
         return [(w.batch, w.head, w.tile, w.split) for w in out[:n]]
     return [(w.batch, w.head, w.tile) for w in out[:n]]
+
+
+def key_range(p: Params, tile, split, seqlen_k):
+    """Keys (begin, end) of one sequence of ``seqlen_k`` keys that split-KV
+    range ``split`` of query tile ``tile`` covers (attn_fwd_key_range)."""
+    b, e = ctypes.c_int32(), ctypes.c_int32()
+    st = lib().attn_fwd_key_range(ctypes.byref(p), int(tile), int(split), int(seqlen_k), ctypes.byref(b),
+                                  ctypes.byref(e))
+    if st != ATTN_OK:
+        raise AttnError(st, last_error())
+    return b.value, e.value

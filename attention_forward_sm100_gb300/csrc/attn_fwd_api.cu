@@ -60,7 +60,8 @@ attn_status validate(const attn_fwd_params* p) {
   if (p->num_splits >= 2) {
     if (p->backend != ATTN_BACKEND_TCGEN05)
       return fail(ATTN_ERR_UNSUPPORTED, "split-KV runs on the tcgen05 backend only");
-    if (p->causal) return fail(ATTN_ERR_UNSUPPORTED, "split-KV is not supported with the causal mask");
+    if (p->causal && p->pair_cta == ATTN_PAIR_ON)
+      return fail(ATTN_ERR_UNSUPPORTED, "causal split-KV is not supported with CTA pairs");
   }
   if (p->batch < 0 || p->seqlen_q < 0 || p->seqlen_k < 0 || p->total_q < 0 || p->total_k < 0)
     return fail(ATTN_ERR_INVALID_ARG, "negative size");
@@ -227,15 +228,19 @@ int64_t work_tiles_bound(const attn_fwd_params* p) {
 
 // Key ranges per query tile for `p` (1 = no split-KV). Explicit counts are
 // capped at the number of key tiles (of the longest sequence when packed);
-// 0 asks for the scheduler's choice on unmasked problems (for packed
-// sequences from the upper bound of the query tiles, B * ceil(max_len / rows)).
+// 0 asks for the scheduler's choice (for packed sequences from the longest
+// lengths and the upper bound of the query tiles, B * ceil(max_len / rows)).
+// Causal problems on CTA pairs do not split.
 int32_t resolve_splits(const attn_fwd_params* p) {
   if (p == nullptr || p->num_splits == 1 || p->num_splits < 0 || p->num_splits > af::kMaxSplits ||
-      p->backend != ATTN_BACKEND_TCGEN05 || p->causal || p->batch <= 0 || p->seqlen_q <= 0 ||
+      p->backend != ATTN_BACKEND_TCGEN05 || (p->causal && use_pair(p)) || p->batch <= 0 || p->seqlen_q <= 0 ||
       p->seqlen_k <= 0 || p->num_heads_q <= 0 || (p->cu_seqlens_q != nullptr && p->total_q <= 0))
     return 1;
   const int32_t kv_tiles = af::tiles_for(p->seqlen_k, af::kBlockN);
   if (p->num_splits >= 2) return p->num_splits < kv_tiles ? p->num_splits : kv_tiles;
+  if (p->causal)
+    return af::choose_splits_causal((int64_t)p->batch * p->num_heads_q, p->seqlen_q, p->seqlen_k, rows_for(p),
+                                    af::kBlockM, af::kBlockN, p->head_dim_v, persistent_units(p), af::kMaxSplits);
   return af::choose_splits(work_tiles_bound(p), kv_tiles, persistent_units(p), af::kMaxSplits);
 }
 
@@ -609,6 +614,32 @@ int64_t attn_fwd_schedule(const attn_fwd_params* p, const int32_t* host_cu_seqle
     }
   }
   return n;
+}
+
+attn_status attn_fwd_key_range(const attn_fwd_params* p, int32_t tile, int32_t split, int32_t seqlen_k,
+                               int32_t* key_begin, int32_t* key_end) {
+  clear_error();
+  if (p == nullptr || key_begin == nullptr || key_end == nullptr)
+    return fail(ATTN_ERR_INVALID_ARG, "NULL argument");
+  if (tile < 0 || seqlen_k < 0) return fail(ATTN_ERR_INVALID_ARG, "tile %d / seqlen_k %d negative", tile, seqlen_k);
+  const int32_t splits = resolve_splits(p);
+  if (split < 0 || split >= splits) return fail(ATTN_ERR_INVALID_ARG, "split %d outside [0, %d)", split, splits);
+  if (splits == 1) {
+    *key_begin = 0;
+    *key_end = seqlen_k;
+    return ATTN_OK;
+  }
+  const int32_t rows = rows_for(p);
+  if ((int64_t)tile * rows > 0x7fffffffll - rows) return fail(ATTN_ERR_INVALID_ARG, "tile %d too large", tile);
+  int32_t j0 = 0, j1 = 0;
+  if (p->causal)
+    af::causal_split_range(split, splits, tile * rows, af::kBlockM, rows, seqlen_k, af::kBlockN, &j0, &j1);
+  else
+    af::split_range(split, splits, af::tiles_for(seqlen_k, af::kBlockN), &j0, &j1);
+  const int64_t b = (int64_t)j0 * af::kBlockN, e = (int64_t)j1 * af::kBlockN;
+  *key_begin = (int32_t)(b < seqlen_k ? b : seqlen_k);
+  *key_end = (int32_t)(e < seqlen_k ? e : seqlen_k);
+  return ATTN_OK;
 }
 
 const char* attn_status_string(attn_status s) {

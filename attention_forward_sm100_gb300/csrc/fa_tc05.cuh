@@ -191,6 +191,7 @@ struct Tc05Traits {
 struct SchedSlot {
   int32_t valid, b, h, t, q_start, lq, k_start, lk, split;
   int32_t v_start;   // first key of the tile's range along V's key dimension (packed e4m3 V: own offsets)
+  int32_t koff;      // first key of the range within its sequence (0 without split-KV): the causal mask
 };
 
 struct Ctx {
@@ -305,17 +306,21 @@ __device__ __forceinline__ Geo tile_geo(const SchedSlot& s, uint32_t rank) {
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     g.row[i] = g.q0 + T::MMA_M * i + kBlockM * (int)rank;
-    const int kv_end = CAUSAL ? min(s.lk, g.q0 + T::MMA_M * (i + 1)) : s.lk;
+    // causal: keys up to the tile's last row, counted from the range's first key
+    const int kv_end = CAUSAL ? min(s.lk, g.q0 + T::MMA_M * (i + 1) - s.koff) : s.lk;
     g.n[i] = kv_end > 0 ? (kv_end + kBlockN - 1) / kBlockN : 0;
   }
   return g;
 }
 
+// The range's key offset travels only in causal kernels (the only users).
+template <bool CAUSAL>
 __device__ __forceinline__ SchedSlot read_slot(const Ctx& c, int slot, int off_sched) {
   const volatile int32_t* p = reinterpret_cast<const volatile int32_t*>(c.smem + off_sched + kSlotBytes * slot);
   SchedSlot s;
   s.valid = p[0]; s.b = p[1]; s.h = p[2]; s.t = p[3];
   s.q_start = p[4]; s.lq = p[5]; s.k_start = p[6]; s.lk = p[7]; s.split = p[8]; s.v_start = p[9];
+  s.koff = CAUSAL ? p[10] : 0;
   return s;
 }
 
@@ -326,10 +331,11 @@ struct Cursor {
   int64_t base = 0;
 };
 
+template <bool CAUSAL>
 __device__ __forceinline__ SchedSlot decode_work(const Tc05Params& P, int64_t w, Cursor& cur) {
   SchedSlot s;
   s.valid = 0;
-  s.b = s.h = s.t = s.q_start = s.k_start = s.split = s.v_start = 0;
+  s.b = s.h = s.t = s.q_start = s.k_start = s.split = s.v_start = s.koff = 0;
   s.lq = P.seqlen_q;
   s.lk = P.seqlen_k;
   if (!P.packed) {
@@ -338,9 +344,14 @@ __device__ __forceinline__ SchedSlot decode_work(const Tc05Params& P, int64_t w,
       s.valid = 1; s.b = wt.b; s.h = wt.h; s.t = wt.t; s.split = wt.split;
       if (P.num_splits > 1) {
         int32_t j0, j1;
-        split_range(wt.split, P.num_splits, P.kv_tiles, &j0, &j1);
+        if (CAUSAL)
+          causal_split_range(wt.split, P.num_splits, wt.t * P.rows_per_tile, kBlockM, P.rows_per_tile, P.seqlen_k,
+                             kBlockN, &j0, &j1);
+        else
+          split_range(wt.split, P.num_splits, P.kv_tiles, &j0, &j1);
         s.k_start = j0 * kBlockN;
         s.lk = min(P.seqlen_k, j1 * kBlockN) - s.k_start;
+        if (CAUSAL) s.koff = s.k_start;
       }
       s.v_start = s.k_start;
     }
@@ -394,9 +405,14 @@ __device__ __forceinline__ SchedSlot decode_work(const Tc05Params& P, int64_t w,
         s.split = wt.t % P.num_splits;
         s.t = wt.t / P.num_splits;
         int32_t j0, j1;
-        split_range(s.split, P.num_splits, tiles_for(ke - ks, kBlockN), &j0, &j1);
+        if (CAUSAL)
+          causal_split_range(s.split, P.num_splits, s.t * P.rows_per_tile, kBlockM, P.rows_per_tile, ke - ks,
+                             kBlockN, &j0, &j1);
+        else
+          split_range(s.split, P.num_splits, tiles_for(ke - ks, kBlockN), &j0, &j1);
         s.k_start = ks + j0 * kBlockN;
         s.lk = min(ke - ks, j1 * kBlockN) - j0 * kBlockN;
+        if (CAUSAL) s.koff = j0 * kBlockN;
       }
       s.v_start = P.cu_v != nullptr ? P.cu_v[b] + (s.k_start - ks) : s.k_start;
       return s;
@@ -446,12 +462,13 @@ __device__ void role_load_qk(const Tc05Params& P, const Ctx& c) {
   const int64_t units = T::PAIR ? (int64_t)ptx::nclusters_x() : (int64_t)gridDim.x;
   bool aborted = false;
   while (true) {
-    const SchedSlot s = decode_work(P, w, cur);
+    const SchedSlot s = decode_work<CAUSAL>(P, w, cur);
     if (!wait_warp(c, BAR_SCHED_EMPTY + sched.idx, sched.phase ^ 1u, kRoleLoadQK)) { aborted = true; break; }
     if (lane == 0) {
       volatile int32_t* p = reinterpret_cast<volatile int32_t*>(c.smem + T::OFF_SCHED + kSlotBytes * sched.idx);
       p[0] = s.valid; p[1] = s.b; p[2] = s.h; p[3] = s.t;
       p[4] = s.q_start; p[5] = s.lq; p[6] = s.k_start; p[7] = s.lk; p[8] = s.split; p[9] = s.v_start;
+      if (CAUSAL) p[10] = s.koff;
       ptx::mbar_arrive(c.bar(BAR_SCHED_FULL + sched.idx));
     }
     __syncwarp();
@@ -568,7 +585,7 @@ __device__ void role_load_v(const Tc05Params& P, const Ctx& c) {
   bool aborted = false;
   while (true) {
     if (!wait_warp(c, BAR_SCHED_FULL + sched.idx, sched.phase, kRoleLoadV)) { aborted = true; break; }
-    const SchedSlot s = read_slot(c, sched.idx, T::OFF_SCHED);
+    const SchedSlot s = read_slot<CAUSAL>(c, sched.idx, T::OFF_SCHED);
     if (lane == 0) ptx::mbar_arrive(c.bar(BAR_SCHED_EMPTY + sched.idx));
     sched.next();
     if (!s.valid) break;
@@ -712,7 +729,7 @@ __device__ void role_mma(const Tc05Params& P, const Ctx& c, const int i) {
   }
   while (true) {
     if (!wait_one(c, BAR_SCHED_FULL + sched.idx, sched.phase, role)) { aborted = true; break; }
-    const SchedSlot s = read_slot(c, sched.idx, T::OFF_SCHED);
+    const SchedSlot s = read_slot<CAUSAL>(c, sched.idx, T::OFF_SCHED);
     ptx::mbar_arrive(c.bar(BAR_SCHED_EMPTY + sched.idx));
     sched.next();
     if (!s.valid) break;
@@ -804,7 +821,7 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
   const uint32_t turn_flip = i == 0 ? 1u : 0u;   // warpgroup 0 takes the first turn
   while (true) {
     if (!wait_warp(c, BAR_SCHED_FULL + sched.idx, sched.phase, role)) return;
-    const SchedSlot s = read_slot(c, sched.idx, T::OFF_SCHED);
+    const SchedSlot s = read_slot<CAUSAL>(c, sched.idx, T::OFF_SCHED);
     ptx::mbar_arrive(c.bar(BAR_SCHED_EMPTY + sched.idx));
     sched.next();
     if (!s.valid) return;
@@ -812,12 +829,14 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
     const int n = g.n[i];
     const int qi = g.row[i] + tid;               // row within the sequence
     const bool row_valid = qi < s.lq;
-    const int lim = CAUSAL ? min(s.lk, qi + 1) : s.lk;   // keys visible to this row
+    // keys of the range visible to this row (causal: keys 0..qi of the
+    // sequence, the range starting at key koff of it)
+    const int lim = CAUSAL ? min(s.lk, qi + 1 - s.koff) : s.lk;
     const int first_row = g.row[i];
     // LSE element: [B][Hq][Sq] (or [Hq][Tq] packed); a split-KV range writes
     // its partial LSE to copy `split` of that layout, [split][B][Hq][Sq] (or
     // [split][Hq][Tq]).
-    const bool split_kv = !CAUSAL && P.num_splits > 1;   // the host never splits a causal problem
+    const bool split_kv = P.num_splits > 1;
     const int sp = split_kv ? s.split : 0;
     const int64_t lse_idx = P.packed ? ((int64_t)sp * P.heads_q + s.h) * P.total_q + s.q_start + qi
                                      : (((int64_t)sp * P.batch + s.b) * P.heads_q + s.h) * P.seqlen_q + qi;
@@ -874,7 +893,7 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
           sv[2 * e + 1] = a1;
         }
       }
-      const bool need_mask = (kb + kBlockN > s.lk) || (CAUSAL && kb + kBlockN - 1 > first_row);
+      const bool need_mask = (kb + kBlockN > s.lk) || (CAUSAL && s.koff + kb + kBlockN - 1 > first_row);
       if (need_mask) {
         const int vis = lim - kb;
         if constexpr (T::V8) {
@@ -983,7 +1002,7 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
     }
     // Row statistics: LSE (natural log) here, 1/l to the epilogue. A split-KV
     // range writes the LSE of its own keys for the merge.
-    float* const lse_dst = (!CAUSAL && P.num_splits > 1) ? P.lse_part : P.lse;
+    float* const lse_dst = P.num_splits > 1 ? P.lse_part : P.lse;
     if (row_valid && lse_dst != nullptr) {
       const float lse = l > 0.f ? (m + ptx::lg2(l)) * 0.69314718055994531f : -INFINITY;
       lse_dst[lse_idx] = lse;
@@ -1033,7 +1052,7 @@ __device__ void role_correction(const Tc05Params& P, const Ctx& c) {
   uint32_t stats_phase[2] = {0, 0}, ofinal_phase[2] = {0, 0};
   while (true) {
     if (!wait_warp(c, BAR_SCHED_FULL + sched.idx, sched.phase, kRoleCorrection)) return;
-    const SchedSlot s = read_slot(c, sched.idx, T::OFF_SCHED);
+    const SchedSlot s = read_slot<CAUSAL>(c, sched.idx, T::OFF_SCHED);
     ptx::mbar_arrive(c.bar(BAR_SCHED_EMPTY + sched.idx));
     sched.next();
     if (!s.valid) return;
@@ -1054,8 +1073,8 @@ __device__ void role_correction(const Tc05Params& P, const Ctx& c) {
         ofinal_phase[i] ^= 1u;
         ptx::tc_fence_after();
         const uint32_t tO = c.tmem + lane_base + T::tm_o(i);
-        if (!CAUSAL && P.num_splits > 1) {
-          // Split-KV range (never causal): normalised partial O in fp32 for the merge.
+        if (P.num_splits > 1) {
+          // Split-KV range: normalised partial O in fp32 for the merge.
           float* prow = P.o_part + partial_row(P, s, qi) * T::DV;
 #pragma unroll 1
           for (int q = 0; q < T::DV / 32; ++q) {
@@ -1073,8 +1092,9 @@ __device__ void role_correction(const Tc05Params& P, const Ctx& c) {
             if (row_valid) store_row_chunk<T>(orow + 32 * q, r, rl);
           }
         }
-      } else if (row_valid && !CAUSAL && P.num_splits > 1) {
-        // An empty key range (a short packed sequence): a zero partial row
+      } else if (row_valid && P.num_splits > 1) {
+        // An empty key range (a short packed sequence, or under the causal
+        // mask a range this tile's rows do not reach): a zero partial row
         // (its LSE is -inf, so the merge gives it no weight).
         float4* d = reinterpret_cast<float4*>(P.o_part + partial_row(P, s, qi) * T::DV);
 #pragma unroll 1

@@ -305,9 +305,18 @@ def prepare(spec, dev, schedule):
 
 
 def time_calls(step, steps, stream):
-    """Per-call device times (ms) of `steps` calls, CUDA events on `stream`."""
+    """Per-call device times (ms) of `steps` calls, CUDA events on `stream`.
+
+    A short device-side sleep is queued ahead of the first event, so the first
+    call is already enqueued when the GPU reaches it: the first interval then
+    holds that call's device time and not the host's latency to issue it
+    (the first event would otherwise be recorded on an idle GPU). Calls that
+    take less device time than the host needs to issue one stay host-bound
+    after the first."""
     import torch
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(200_000)          # ~0.1 ms at ~2 GHz: longer than one host call
     ev[0].record(stream)
     for i in range(steps):
         step()
@@ -401,8 +410,7 @@ def time_other_workloads(args, dev, stream, peaks, peak_src):
         pkg.check(device=dev)
         clocks = ClockSampler(dev.index if dev.index is not None else 0)
         clocks.start()
-        time.sleep(0.2)
-        torch.cuda.synchronize(dev)
+        soak(step, dev, 0.2)        # the same calls keep the clocks up while the sampler starts
         per_call, _ = time_calls(step, args.steps, stream)
         soak(step, dev, 0.6)
         clk = clocks.stop()
@@ -490,7 +498,7 @@ def main():
 
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
-    time.sleep(0.3)
+    soak(step, dev, 0.3)            # the same calls keep the clocks up while the sampler starts
     barrier(world)
     torch.cuda.synchronize(dev)
     per_launch, total_ms = time_calls(step, args.steps, stream)

@@ -156,13 +156,16 @@ typedef struct attn_fwd_params {
 
   /* Split-KV: number of key ranges each query tile is split into (the
    * "splitk_partitions" of the SM100AttentionSMem page's configuration).
-   * 0 = chosen by the library (splits only unmasked problems with too few
-   * query tiles to fill the GPU), 1 = off, n >= 2 = n ranges (at most 64,
-   * capped at the key tiles of the longest sequence; a packed sequence with
-   * fewer key tiles leaves some of its ranges empty). Each range writes a
-   * normalised partial O and its LSE into the workspace
-   * (attn_fwd_workspace_bytes grows accordingly) and a second small kernel
-   * merges them. Causal problems do not split (UNSUPPORTED if n >= 2). */
+   * 0 = chosen by the library (splits problems whose query tiles cannot
+   * fill the GPU: unmasked problems with too few query tiles, causal
+   * problems whose heaviest query tile outlasts the rest of the work),
+   * 1 = off, n >= 2 = n ranges (at most 64, capped at the key tiles of the
+   * longest sequence; a sequence or, under the causal mask, a query tile
+   * with fewer key tiles leaves some of its ranges empty; attn_fwd_key_range
+   * gives each range's keys). Each range writes a normalised partial O and
+   * its LSE into the workspace (attn_fwd_workspace_bytes grows accordingly)
+   * and a second small kernel merges them. Causal split-KV with CTA pairs is
+   * UNSUPPORTED (n >= 2); the automatic choice does not split there. */
   int32_t num_splits;
 
   /* attn_schedule; ignored by the simple backend. */
@@ -263,6 +266,23 @@ attn_status attn_fwd_plan(const attn_fwd_params *p, attn_fwd_plan_info *out);
  * for fixed length. Used to test the schedule on a CPU. */
 int64_t attn_fwd_schedule(const attn_fwd_params *p, const int32_t *host_cu_seqlens_q,
                           attn_work_tile *out, int64_t cap);
+
+/* Keys [*key_begin, *key_end) of one sequence (seqlen_k keys) that range
+ * `split` of query tile `tile` covers, as the kernel computes them (split-KV,
+ * the "splitk_partitions" of the SM100AttentionSMem page's configuration).
+ * Without split-KV the range is the whole sequence. Unmasked, the ranges cut
+ * the sequence's key tiles into num_splits contiguous parts. Under the
+ * causal mask they cut the key tiles the query tile's first 128 rows see, and
+ * the last range also takes the tiles only its later rows see: every range
+ * that holds keys starts at or before the tile's first row, and the ranges
+ * end where the tile's last row stops seeing keys (the mask applies within a
+ * range as without split-KV). A range may be empty (*key_begin == *key_end)
+ * when the tile sees fewer key tiles than there are ranges. Host only: the
+ * split count is resolved as attn_fwd_plan reports it. Returns INVALID_ARG
+ * for a NULL pointer, tile < 0, seqlen_k < 0 or split outside
+ * [0, num_splits). */
+attn_status attn_fwd_key_range(const attn_fwd_params *p, int32_t tile, int32_t split, int32_t seqlen_k,
+                               int32_t *key_begin, int32_t *key_end);
 
 /* Static description of a status code. */
 const char *attn_status_string(attn_status s);

@@ -169,7 +169,8 @@ def test_schedule_packed(pkg):
 
 
 # ---------------------------------------------------------------- split-KV
-def _split_params(pkg, B=1, Sq=256, Sk=32768, Hq=32, Hkv=8, causal=False, splits=0, ws_bytes=1 << 30, packed=False):
+def _split_params(pkg, B=1, Sq=256, Sk=32768, Hq=32, Hkv=8, causal=False, splits=0, ws_bytes=1 << 30, packed=False,
+                  pair_cta="auto"):
     q = _Fake((B, Sq, Hq, 128), ptr=1 << 20)
     k = _Fake((B, Sk, Hkv, 128), ptr=2 << 20)
     v = _Fake((B, Sk, Hkv, 128), ptr=3 << 20)
@@ -183,7 +184,8 @@ def _split_params(pkg, B=1, Sq=256, Sk=32768, Hq=32, Hkv=8, causal=False, splits
         o = _Fake((B * Sq, Hq, 128), ptr=4 << 20)
         kw = dict(cu_seqlens_q=_Fake((B + 1,), ptr=6 << 20), cu_seqlens_k=_Fake((B + 1,), ptr=7 << 20),
                   max_seqlen_q=Sq, max_seqlen_k=Sk)
-    return pkg.make_params(q, k, v, causal=causal, out=o, lse=None, workspace=ws, num_splits=splits, **kw)
+    return pkg.make_params(q, k, v, causal=causal, out=o, lse=None, workspace=ws, num_splits=splits,
+                           pair_cta=pair_cta, **kw)
 
 
 def test_split_kv_explicit_plan_and_workspace(pkg):
@@ -206,7 +208,8 @@ def test_split_kv_automatic_choice(pkg):
     auto = pkg.plan(_split_params(pkg)).num_splits
     assert 2 <= auto <= 64
     # ... so does a packed one (from the bound B * ceil(max_len / 256) of its
-    # query tiles); one with many query tiles or a causal one does not.
+    # query tiles); one with many query tiles does not, nor a causal one
+    # whose 256 query rows see at most 256 keys (top-left mask).
     assert pkg.plan(_split_params(pkg, packed=True)).num_splits == auto
     assert pkg.plan(_split_params(pkg, B=4, Sq=4096, Sk=4096, Hq=16, Hkv=16)).num_splits == 1
     assert pkg.plan(_split_params(pkg, causal=True)).num_splits == 1
@@ -215,11 +218,84 @@ def test_split_kv_automatic_choice(pkg):
     assert pkg.plan(_split_params(pkg, Sk=100)).num_splits == 1
 
 
-@pytest.mark.parametrize("case,status", [("causal", 2), ("simple", 2), ("too_many", 1),
+def test_causal_split_kv_automatic_choice(pkg):
+    # One long causal sequence with few heads: the last query tile sees every
+    # key, the first almost none; its 32 x H tiles leave most SMs idle, so
+    # the keys split. The causal bench shape (B4 H16 S4096, 1024 tiles) and a
+    # long sequence with enough heads (B1 H16 S16384) do not.
+    for heads in (1, 2, 4):
+        p = _split_params(pkg, B=1, Sq=8192, Sk=8192, Hq=heads, Hkv=heads, causal=True)
+        assert pkg.plan(p).num_splits >= 2, heads
+        assert pkg.workspace_bytes(p) > 256
+    assert pkg.plan(_split_params(pkg, B=4, Sq=4096, Sk=4096, Hq=16, Hkv=16, causal=True)).num_splits == 1
+    assert pkg.plan(_split_params(pkg, B=1, Sq=16384, Sk=16384, Hq=16, Hkv=16, causal=True)).num_splits == 1
+    # CTA pairs never split a causal problem
+    p = _split_params(pkg, B=1, Sq=8192, Sk=8192, Hq=1, Hkv=1, causal=True, pair_cta="on")
+    assert pkg.plan(p).num_splits == 1
+
+
+def test_causal_split_kv_explicit_plan(pkg):
+    p = _split_params(pkg, B=2, Sq=1000, Sk=1000, Hq=4, Hkv=2, causal=True, splits=3)
+    info = pkg.plan(p)
+    assert info.num_splits == 3
+    assert info.work_tiles == 2 * 4 * 4 * 3          # B * Hq * ceil(1000/256) * splits
+
+
+def _ranges(pkg, p, tile, n, sk):
+    return [pkg.key_range(p, tile, r, sk) for r in range(n)]
+
+
+@pytest.mark.parametrize("sq,sk,splits", [(1000, 1000, 3), (8192, 8192, 7), (300, 5000, 4), (5000, 300, 4),
+                                          (129, 129, 64), (2048, 2048, 2), (640, 700, 5)])
+def test_causal_key_ranges(pkg, sq, sk, splits):
+    """Causal ranges: contiguous, in order, on 128-key boundaries, together
+    exactly the keys the tile's last row sees (top-left mask), and every range
+    that holds keys starts at or before the tile's first row (so its first
+    MMA tile visits it and every row sees its first key)."""
+    p = _split_params(pkg, B=1, Sq=sq, Sk=sk, Hq=2, Hkv=2, causal=True, splits=splits)
+    n = pkg.plan(p).num_splits
+    assert n == min(splits, (sk + 127) // 128)
+    for t in range((sq + 255) // 256):
+        q0 = 256 * t
+        rs = _ranges(pkg, p, t, n, sk)
+        assert rs[0][0] == 0 and rs[-1][1] == min(sk, q0 + 256), (t, rs)
+        for (b0, e0), (b1, e1) in zip(rs, rs[1:]):
+            assert e0 == b1
+        for b, e in rs:
+            assert b <= e and b % 128 == 0
+            if e > b:
+                assert b <= q0, (t, rs)
+        # the pieces are balanced over the first MMA tile's key tiles
+        sizes = [(e - b + 127) // 128 for b, e in rs[:-1]]
+        if sizes:
+            assert max(sizes) - min(sizes) <= 1, rs
+
+
+@pytest.mark.parametrize("sk,splits", [(1000, 3), (32768, 64), (300, 9)])
+def test_unmasked_key_ranges(pkg, sk, splits):
+    p = _split_params(pkg, B=1, Sq=256, Sk=sk, Hq=2, Hkv=2, splits=splits)
+    n = pkg.plan(p).num_splits
+    rs = _ranges(pkg, p, 0, n, sk)
+    assert rs[0][0] == 0 and rs[-1][1] == sk
+    assert all(e0 == b1 for (_, e0), (b1, _) in zip(rs, rs[1:]))
+    assert all(e > b for b, e in rs)                     # n <= key tiles: none empty
+    assert _ranges(pkg, p, 5, n, sk) == rs               # the same for every query tile
+
+
+def test_key_range_without_split_and_rejections(pkg):
+    p = _split_params(pkg, B=1, Sq=256, Sk=1000, Hq=2, Hkv=2, splits=1)
+    assert pkg.key_range(p, 0, 0, 1000) == (0, 1000)
+    for tile, split, sk in ((-1, 0, 10), (0, 1, 10), (0, -1, 10), (0, 0, -1)):
+        with pytest.raises(pkg.AttnError) as e:
+            pkg.key_range(p, tile, split, sk)
+        assert e.value.status == 1
+
+
+@pytest.mark.parametrize("case,status", [("causal_pairs", 2), ("simple", 2), ("too_many", 1),
                                          ("negative", 1), ("small_workspace", 1)])
 def test_split_kv_rejections(pkg, case, status):
-    if case == "causal":
-        p = _split_params(pkg, causal=True, splits=2)
+    if case == "causal_pairs":
+        p = _split_params(pkg, causal=True, splits=2, pair_cta="on")
     elif case == "simple":
         p = _split_params(pkg, splits=2)
         p.backend = 1
@@ -234,10 +310,11 @@ def test_split_kv_rejections(pkg, case, status):
     assert e.value.status == status
 
 
-@pytest.mark.parametrize("B,Sq,Hq,Hkv,Sk,splits", [(1, 256, 32, 8, 32768, 0), (2, 700, 4, 2, 1000, 3),
-                                                    (1, 1, 2, 1, 5000, 64)])
-def test_schedule_with_splits_covers_each_piece_once(pkg, B, Sq, Hq, Hkv, Sk, splits):
-    p = _split_params(pkg, B=B, Sq=Sq, Sk=Sk, Hq=Hq, Hkv=Hkv, splits=splits)
+@pytest.mark.parametrize("B,Sq,Hq,Hkv,Sk,splits,causal", [(1, 256, 32, 8, 32768, 0, False), (2, 700, 4, 2, 1000, 3, False),
+                                                           (1, 1, 2, 1, 5000, 64, False), (2, 700, 4, 2, 1000, 3, True),
+                                                           (1, 8192, 2, 2, 8192, 0, True)])
+def test_schedule_with_splits_covers_each_piece_once(pkg, B, Sq, Hq, Hkv, Sk, splits, causal):
+    p = _split_params(pkg, B=B, Sq=Sq, Sk=Sk, Hq=Hq, Hkv=Hkv, splits=splits, causal=causal)
     n = pkg.plan(p).num_splits
     assert n > 1
     order = pkg.schedule(p, with_split=True)

@@ -1,8 +1,8 @@
 """Seeded random configurations through the tcgen05 kernel against the
 oracle: batch, lengths (fixed, or packed with drawn lengths including 1 and
 exact tile multiples), head counts and GQA ratio, head-dimension variant
-(d64, d128, d128 + rope 64, FP8 Q/K, all-FP8), mask, split-KV count and
-schedule are drawn together, so combinations no hand-written case names get
+(d64, d128, d128 + rope 64, FP8 Q/K, all-FP8), mask, split-KV count (with
+or without the mask) and schedule are drawn together, so combinations no hand-written case names get
 run."""
 import numpy as np
 import pytest
@@ -31,12 +31,12 @@ def _draw_case(seed):
         lk = lens if causal or not rng.integers(2) else [int(rng.integers(1, 600)) for _ in range(b)]
         spec = W.AttnSpec(b, hq, hkv, max(lens), max(lk), d, d, causal, seed=2000 + seed, lengths_q=tuple(lens),
                           lengths_k=tuple(lk), **kw)
-        splits = 1 if causal else int(rng.choice([0, 1, 3]))
+        splits = int(rng.choice([0, 1, 3]))
     else:
         sq = lens[0]
         sk = sq if causal else int(rng.choice([sq, int(rng.integers(1, 1200))]))
         spec = W.AttnSpec(b, hq, hkv, sq, sk, d, d, causal, seed=2000 + seed, **kw)
-        splits = 1 if causal else int(rng.choice([0, 1, 2, 5]))
+        splits = int(rng.choice([0, 1, 2, 5]))
     schedule = str(rng.choice(["dynamic", "static", "grid"]))
     return spec, splits, schedule
 
