@@ -459,7 +459,8 @@ attn_status launch_tc05(const attn_fwd_params* p, cudaStream_t stream) {
   if (grid_for(p, bound) > 0x7fffffffll) return fail(ATTN_ERR_UNSUPPORTED, "too many work tiles for one grid");
   const int grid = (int)grid_for(p, bound);
   prm.schedule = p->schedule;
-  cudaError_t e = af::tc05_launch(variant, p->causal != 0, prm, grid, stream);
+  const int mask = p->causal == 0 ? af::kMaskNone : (splits > 1 ? af::kMaskCausalSplit : af::kMaskCausal);
+  cudaError_t e = af::tc05_launch(variant, mask, prm, grid, stream);
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "tcgen05 kernel launch failed: %s", cudaGetErrorString(e));
   if (splits > 1) {
     af::SplitCombineParams cp;

@@ -299,7 +299,7 @@ struct Geo {
   int n[2];     // K/V tiles MMA tile i visits
 };
 
-template <class T, bool CAUSAL>
+template <class T, int CAUSAL>
 __device__ __forceinline__ Geo tile_geo(const SchedSlot& s, uint32_t rank) {
   Geo g;
   g.q0 = s.t * T::ROWS_PER_WORK;
@@ -313,14 +313,22 @@ __device__ __forceinline__ Geo tile_geo(const SchedSlot& s, uint32_t rank) {
   return g;
 }
 
-// The range's key offset travels only in causal kernels (the only users).
-template <bool CAUSAL>
+// Whether this kernel flavour runs split-KV ranges: the unmasked kernels
+// decide at run time, the causal flavour never (its split code compiles
+// out), the causal split flavour always.
+template <int CAUSAL>
+__device__ __forceinline__ bool splits_keys(const Tc05Params& P) {
+  return CAUSAL == kMaskCausal ? false : (CAUSAL == kMaskCausalSplit ? true : P.num_splits > 1);
+}
+
+// The range's key offset travels only in the causal split flavour (its only user).
+template <int CAUSAL>
 __device__ __forceinline__ SchedSlot read_slot(const Ctx& c, int slot, int off_sched) {
   const volatile int32_t* p = reinterpret_cast<const volatile int32_t*>(c.smem + off_sched + kSlotBytes * slot);
   SchedSlot s;
   s.valid = p[0]; s.b = p[1]; s.h = p[2]; s.t = p[3];
   s.q_start = p[4]; s.lq = p[5]; s.k_start = p[6]; s.lk = p[7]; s.split = p[8]; s.v_start = p[9];
-  s.koff = CAUSAL ? p[10] : 0;
+  s.koff = CAUSAL == kMaskCausalSplit ? p[10] : 0;
   return s;
 }
 
@@ -331,7 +339,7 @@ struct Cursor {
   int64_t base = 0;
 };
 
-template <bool CAUSAL>
+template <int CAUSAL>
 __device__ __forceinline__ SchedSlot decode_work(const Tc05Params& P, int64_t w, Cursor& cur) {
   SchedSlot s;
   s.valid = 0;
@@ -342,7 +350,7 @@ __device__ __forceinline__ SchedSlot decode_work(const Tc05Params& P, int64_t w,
     if (w < P.total_work) {
       const WorkTile wt = decode_fixed(w, P.tiles_per_seq, P.num_splits, P.heads_q, P.group, P.kv_chunk);
       s.valid = 1; s.b = wt.b; s.h = wt.h; s.t = wt.t; s.split = wt.split;
-      if (P.num_splits > 1) {
+      if (splits_keys<CAUSAL>(P)) {
         int32_t j0, j1;
         if (CAUSAL)
           causal_split_range(wt.split, P.num_splits, wt.t * P.rows_per_tile, kBlockM, P.rows_per_tile, P.seqlen_k,
@@ -351,7 +359,7 @@ __device__ __forceinline__ SchedSlot decode_work(const Tc05Params& P, int64_t w,
           split_range(wt.split, P.num_splits, P.kv_tiles, &j0, &j1);
         s.k_start = j0 * kBlockN;
         s.lk = min(P.seqlen_k, j1 * kBlockN) - s.k_start;
-        if (CAUSAL) s.koff = s.k_start;
+        if (CAUSAL == kMaskCausalSplit) s.koff = s.k_start;
       }
       s.v_start = s.k_start;
     }
@@ -399,7 +407,7 @@ __device__ __forceinline__ SchedSlot decode_work(const Tc05Params& P, int64_t w,
                                              P.group, P.heads_kv, P.kv_chunk);
       s.valid = 1; s.b = b; s.h = wt.h; s.t = wt.t;
       s.q_start = qs; s.lq = qe - qs; s.k_start = ks; s.lk = ke - ks;
-      if (P.num_splits > 1) {
+      if (splits_keys<CAUSAL>(P)) {
         // this sequence's own key tiles, cut like the fixed-length case (a
         // range can be empty when the sequence has fewer key tiles than ranges)
         s.split = wt.t % P.num_splits;
@@ -412,7 +420,7 @@ __device__ __forceinline__ SchedSlot decode_work(const Tc05Params& P, int64_t w,
           split_range(s.split, P.num_splits, tiles_for(ke - ks, kBlockN), &j0, &j1);
         s.k_start = ks + j0 * kBlockN;
         s.lk = min(ke - ks, j1 * kBlockN) - j0 * kBlockN;
-        if (CAUSAL) s.koff = j0 * kBlockN;
+        if (CAUSAL == kMaskCausalSplit) s.koff = j0 * kBlockN;
       }
       s.v_start = P.cu_v != nullptr ? P.cu_v[b] + (s.k_start - ks) : s.k_start;
       return s;
@@ -442,7 +450,7 @@ __device__ __forceinline__ void pair_copy_grace() {
   }
 }
 
-template <class T, bool CAUSAL>
+template <class T, int CAUSAL>
 __device__ void role_load_qk(const Tc05Params& P, const Ctx& c) {
   const int lane = threadIdx.x & 31;
   const bool lead = c.rank == 0;
@@ -468,7 +476,7 @@ __device__ void role_load_qk(const Tc05Params& P, const Ctx& c) {
       volatile int32_t* p = reinterpret_cast<volatile int32_t*>(c.smem + T::OFF_SCHED + kSlotBytes * sched.idx);
       p[0] = s.valid; p[1] = s.b; p[2] = s.h; p[3] = s.t;
       p[4] = s.q_start; p[5] = s.lq; p[6] = s.k_start; p[7] = s.lk; p[8] = s.split; p[9] = s.v_start;
-      if (CAUSAL) p[10] = s.koff;
+      if (CAUSAL == kMaskCausalSplit) p[10] = s.koff;
       ptx::mbar_arrive(c.bar(BAR_SCHED_FULL + sched.idx));
     }
     __syncwarp();
@@ -571,7 +579,7 @@ __device__ void role_load_qk(const Tc05Params& P, const Ctx& c) {
   __syncwarp();
 }
 
-template <class T, bool CAUSAL>
+template <class T, int CAUSAL>
 __device__ void role_load_v(const Tc05Params& P, const Ctx& c) {
   const int lane = threadIdx.x & 31;
   const bool lead = c.rank == 0;
@@ -704,7 +712,7 @@ __device__ __forceinline__ void commit(const Ctx& c, int id) {
   else ptx::mma_commit(c.bar(id));
 }
 
-template <class T, bool CAUSAL>
+template <class T, int CAUSAL>
 __device__ void role_mma(const Tc05Params& P, const Ctx& c, const int i) {
   // Runs on lane 0 of warp 12 + i only (in a pair: of the first CTA): one
   // thread issues, waits and commits.
@@ -807,7 +815,7 @@ __device__ void role_mma(const Tc05Params& P, const Ctx& c, const int i) {
 }
 
 // ---------------------------------------------------------------------------------------------
-template <class T, bool CAUSAL>
+template <class T, int CAUSAL>
 __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
   const int tid = threadIdx.x - 128 * i;          // row of the Q tile == TMEM lane
   const uint32_t lane_base = (uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16;
@@ -836,7 +844,7 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
     // LSE element: [B][Hq][Sq] (or [Hq][Tq] packed); a split-KV range writes
     // its partial LSE to copy `split` of that layout, [split][B][Hq][Sq] (or
     // [split][Hq][Tq]).
-    const bool split_kv = P.num_splits > 1;
+    const bool split_kv = splits_keys<CAUSAL>(P);
     const int sp = split_kv ? s.split : 0;
     const int64_t lse_idx = P.packed ? ((int64_t)sp * P.heads_q + s.h) * P.total_q + s.q_start + qi
                                      : (((int64_t)sp * P.batch + s.b) * P.heads_q + s.h) * P.seqlen_q + qi;
@@ -1002,7 +1010,7 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
     }
     // Row statistics: LSE (natural log) here, 1/l to the epilogue. A split-KV
     // range writes the LSE of its own keys for the merge.
-    float* const lse_dst = P.num_splits > 1 ? P.lse_part : P.lse;
+    float* const lse_dst = splits_keys<CAUSAL>(P) ? P.lse_part : P.lse;
     if (row_valid && lse_dst != nullptr) {
       const float lse = l > 0.f ? (m + ptx::lg2(l)) * 0.69314718055994531f : -INFINITY;
       lse_dst[lse_idx] = lse;
@@ -1043,7 +1051,7 @@ __device__ __forceinline__ void store_row_chunk_f32(float* dst, const uint32_t (
                        __uint_as_float(r[4 * e + 2]) * scale, __uint_as_float(r[4 * e + 3]) * scale);
 }
 
-template <class T, bool CAUSAL>
+template <class T, int CAUSAL>
 __device__ void role_correction(const Tc05Params& P, const Ctx& c) {
   const int tid = threadIdx.x - 256;
   const uint32_t lane_base = (uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16;
@@ -1073,7 +1081,7 @@ __device__ void role_correction(const Tc05Params& P, const Ctx& c) {
         ofinal_phase[i] ^= 1u;
         ptx::tc_fence_after();
         const uint32_t tO = c.tmem + lane_base + T::tm_o(i);
-        if (P.num_splits > 1) {
+        if (splits_keys<CAUSAL>(P)) {
           // Split-KV range: normalised partial O in fp32 for the merge.
           float* prow = P.o_part + partial_row(P, s, qi) * T::DV;
 #pragma unroll 1
@@ -1092,7 +1100,7 @@ __device__ void role_correction(const Tc05Params& P, const Ctx& c) {
             if (row_valid) store_row_chunk<T>(orow + 32 * q, r, rl);
           }
         }
-      } else if (row_valid && P.num_splits > 1) {
+      } else if (row_valid && splits_keys<CAUSAL>(P)) {
         // An empty key range (a short packed sequence, or under the causal
         // mask a range this tile's rows do not reach): a zero partial row
         // (its LSE is -inf, so the merge gives it no weight).
@@ -1126,7 +1134,7 @@ __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-template <class T, bool CAUSAL>
+template <class T, int CAUSAL>
 __global__ void __launch_bounds__(512, 1) fa_tc05_kernel(const __grid_constant__ Tc05Params P) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Ctx c;
@@ -1292,7 +1300,7 @@ cudaError_t launch_with_smem(int bytes, F launch) {
   return launch();
 }
 
-template <class T, bool CAUSAL>
+template <class T, int CAUSAL>
 cudaError_t tc05_launch_tc(const Tc05Params& prm, int grid, cudaStream_t stream) {
   constexpr auto kern = fa_tc05_kernel<T, CAUSAL>;
   return launch_with_smem<kern>(T::SMEM_BYTES, [&]() -> cudaError_t {
@@ -1310,8 +1318,13 @@ cudaError_t tc05_launch_tc(const Tc05Params& prm, int grid, cudaStream_t stream)
 }
 
 template <class T>
-cudaError_t tc05_launch_t(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream) {
-  return causal ? tc05_launch_tc<T, true>(prm, grid, stream) : tc05_launch_tc<T, false>(prm, grid, stream);
+cudaError_t tc05_launch_t(int mask, const Tc05Params& prm, int grid, cudaStream_t stream) {
+  if (mask == kMaskNone) return tc05_launch_tc<T, kMaskNone>(prm, grid, stream);
+  if (mask == kMaskCausal) return tc05_launch_tc<T, kMaskCausal>(prm, grid, stream);
+  if constexpr (!T::PAIR) {
+    if (mask == kMaskCausalSplit) return tc05_launch_tc<T, kMaskCausalSplit>(prm, grid, stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 // Clusters of a pair variant that can be resident at once on the current
@@ -1321,7 +1334,7 @@ int tc05_max_clusters_t() {
   if constexpr (!T::PAIR) {
     return 0;
   } else {
-    auto kern = fa_tc05_kernel<T, true>;
+    auto kern = fa_tc05_kernel<T, kMaskCausal>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES) != cudaSuccess) {
       cudaGetLastError();
       return 0;
@@ -1356,13 +1369,13 @@ using TraitsFp8QkvD128 = Tc05Traits<128, 0, 128, true, true>;
 using TraitsD128Pair = Tc05Traits<128, 0, 128, false, false, true>;
 using TraitsD128R64Pair = Tc05Traits<128, 64, 128, false, false, true>;
 
-cudaError_t tc05_launch_d64(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
-cudaError_t tc05_launch_d128(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
-cudaError_t tc05_launch_d128r64(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
-cudaError_t tc05_launch_fp8d128(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
-cudaError_t tc05_launch_fp8qkvd128(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
-cudaError_t tc05_launch_d128pair(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
-cudaError_t tc05_launch_d128r64pair(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
+cudaError_t tc05_launch_d64(int mask, const Tc05Params& prm, int grid, cudaStream_t stream);
+cudaError_t tc05_launch_d128(int mask, const Tc05Params& prm, int grid, cudaStream_t stream);
+cudaError_t tc05_launch_d128r64(int mask, const Tc05Params& prm, int grid, cudaStream_t stream);
+cudaError_t tc05_launch_fp8d128(int mask, const Tc05Params& prm, int grid, cudaStream_t stream);
+cudaError_t tc05_launch_fp8qkvd128(int mask, const Tc05Params& prm, int grid, cudaStream_t stream);
+cudaError_t tc05_launch_d128pair(int mask, const Tc05Params& prm, int grid, cudaStream_t stream);
+cudaError_t tc05_launch_d128r64pair(int mask, const Tc05Params& prm, int grid, cudaStream_t stream);
 int tc05_max_clusters_d128pair();
 int tc05_max_clusters_d128r64pair();
 

@@ -104,9 +104,13 @@ attn_status report_error(attn_status st, const char* fmt, ...);
 
 // Static configuration of a variant (host).
 Tc05Config tc05_config(int variant);
+// Mask flavours of the tcgen05 kernel: no mask (split-KV decided at run
+// time), causal without split-KV (its split code compiled out), causal with
+// split-KV (pair variants have none).
+enum Tc05Mask : int { kMaskNone = 0, kMaskCausal = 1, kMaskCausalSplit = 2 };
 // Launch of one variant (defined in the per-variant translation units); a
 // pair variant's grid counts CTAs and must be even.
-cudaError_t tc05_launch(int variant, bool causal, const Tc05Params& prm, int grid, cudaStream_t stream);
+cudaError_t tc05_launch(int variant, int mask, const Tc05Params& prm, int grid, cudaStream_t stream);
 // Pair variants: clusters of two CTAs that fit on the current device at once
 // (0 when unknown).
 int tc05_max_clusters(int variant);

@@ -3,8 +3,8 @@
 #include "fa_tc05.cuh"
 
 namespace af {
-cudaError_t tc05_launch_d128pair(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream) {
-  return tc05_launch_t<TraitsD128Pair>(causal, prm, grid, stream);
+cudaError_t tc05_launch_d128pair(int mask, const Tc05Params& prm, int grid, cudaStream_t stream) {
+  return tc05_launch_t<TraitsD128Pair>(mask, prm, grid, stream);
 }
 int tc05_max_clusters_d128pair() { return tc05_max_clusters_t<TraitsD128Pair>(); }
 }  // namespace af

@@ -2,7 +2,7 @@
 #include "fa_tc05.cuh"
 
 namespace af {
-cudaError_t tc05_launch_d128r64(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream) {
-  return tc05_launch_t<TraitsD128R64>(causal, prm, grid, stream);
+cudaError_t tc05_launch_d128r64(int mask, const Tc05Params& prm, int grid, cudaStream_t stream) {
+  return tc05_launch_t<TraitsD128R64>(mask, prm, grid, stream);
 }
 }  // namespace af

@@ -15,15 +15,15 @@ Tc05Config tc05_config(int variant) {
   }
 }
 
-cudaError_t tc05_launch(int variant, bool causal, const Tc05Params& prm, int grid, cudaStream_t stream) {
+cudaError_t tc05_launch(int variant, int mask, const Tc05Params& prm, int grid, cudaStream_t stream) {
   switch (variant) {
-    case kVarD64: return tc05_launch_d64(causal, prm, grid, stream);
-    case kVarD128: return tc05_launch_d128(causal, prm, grid, stream);
-    case kVarD128Rope64: return tc05_launch_d128r64(causal, prm, grid, stream);
-    case kVarFp8D128: return tc05_launch_fp8d128(causal, prm, grid, stream);
-    case kVarFp8QkvD128: return tc05_launch_fp8qkvd128(causal, prm, grid, stream);
-    case kVarD128Pair: return tc05_launch_d128pair(causal, prm, grid, stream);
-    case kVarD128Rope64Pair: return tc05_launch_d128r64pair(causal, prm, grid, stream);
+    case kVarD64: return tc05_launch_d64(mask, prm, grid, stream);
+    case kVarD128: return tc05_launch_d128(mask, prm, grid, stream);
+    case kVarD128Rope64: return tc05_launch_d128r64(mask, prm, grid, stream);
+    case kVarFp8D128: return tc05_launch_fp8d128(mask, prm, grid, stream);
+    case kVarFp8QkvD128: return tc05_launch_fp8qkvd128(mask, prm, grid, stream);
+    case kVarD128Pair: return tc05_launch_d128pair(mask, prm, grid, stream);
+    case kVarD128Rope64Pair: return tc05_launch_d128r64pair(mask, prm, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

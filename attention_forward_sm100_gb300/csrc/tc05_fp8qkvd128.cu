@@ -2,7 +2,7 @@
 #include "fa_tc05.cuh"
 
 namespace af {
-cudaError_t tc05_launch_fp8qkvd128(bool causal, const Tc05Params& prm, int grid, cudaStream_t stream) {
-  return tc05_launch_t<TraitsFp8QkvD128>(causal, prm, grid, stream);
+cudaError_t tc05_launch_fp8qkvd128(int mask, const Tc05Params& prm, int grid, cudaStream_t stream) {
+  return tc05_launch_t<TraitsFp8QkvD128>(mask, prm, grid, stream);
 }
 }  // namespace af

@@ -126,11 +126,13 @@ def draw_lengths(batch: int, lo: int, hi: int, seed: int) -> list:
     return torch.randint(lo, hi + 1, (batch,), generator=g).tolist()
 
 
-# The workloads, named by what they are. The last two are additions: the
+# The workloads, named by what they are. The last three are additions: the
 # FP8 workload with V rounded to e4m3 as well (same seed, so Q, K and V hold
-# the same draws), and a short-query, long-key shape (a prefill chunk of 256
+# the same draws), a short-query, long-key shape (a prefill chunk of 256
 # rows against a 32k-token cache, GQA 32/8, no mask) whose few query tiles
-# cannot fill the GPU: the shape that split-KV exists for.
+# cannot fill the GPU: the shape that split-KV exists for; and its causal
+# counterpart, one 16k-token sequence with two heads, whose last query tiles
+# see 64 times more keys than the first.
 def _workloads():
     return {
         "mha_b1_h2_s128_d64_noncausal": AttnSpec(
@@ -155,6 +157,9 @@ def _workloads():
         "splitkv_b1_hq32_hkv8_sq256_sk32768_d128_noncausal": AttnSpec(
             batch=1, heads_q=32, heads_kv=8, seqlen_q=256, seqlen_k=32768,
             d_qk=128, d_v=128, causal=False, seed=5),
+        "splitkv_b1_h2_s16384_d128_causal": AttnSpec(
+            batch=1, heads_q=2, heads_kv=2, seqlen_q=16384, seqlen_k=16384,
+            d_qk=128, d_v=128, causal=True, seed=6),
     }
 
 

@@ -268,12 +268,14 @@ def barrier(world):
 
 # The task's workloads timed after the headline one in the same run (GPU
 # only, no CPU leg): the small non-causal case, packed GQA, MLA with the
-# shared rope part and FP8 Q/K; then the two additions (all-FP8 and split-KV);
-# then the d128 and MLA workloads again on CTA pairs (label "+pairs").
+# shared rope part and FP8 Q/K; then the additions (all-FP8, split-KV, and
+# split-KV of one long causal sequence with two heads); then the d128 and MLA
+# workloads again on CTA pairs (label "+pairs").
 OTHER_WORKLOADS = (("mha_b1_h2_s128_d64_noncausal", {}), ("varlen_gqa_b8_hq32_hkv8_d128_causal", {}),
                    ("mla_b2_h128_s4096_d128r64_causal", {}), ("fp8_b2_h32_s8192_d128_causal", {}),
                    ("fp8qkv_b2_h32_s8192_d128_causal", {}),
                    ("splitkv_b1_hq32_hkv8_sq256_sk32768_d128_noncausal", {}),
+                   ("splitkv_b1_h2_s16384_d128_causal", {}),
                    ("mha_b4_h16_s4096_d128_causal", {"pair_cta": "on"}),
                    ("mla_b2_h128_s4096_d128r64_causal", {"pair_cta": "on"}))
 

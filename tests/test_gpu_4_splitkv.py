@@ -91,14 +91,16 @@ def test_split_kv_agrees_with_unsplit(causal):
 
 
 @pytest.mark.gpu
-def test_split_kv_full_workload_sampled_rows():
-    name = "splitkv_b1_hq32_hkv8_sq256_sk32768_d128_noncausal"
+@pytest.mark.parametrize("name", ["splitkv_b1_hq32_hkv8_sq256_sk32768_d128_noncausal",
+                                  "splitkv_b1_h2_s16384_d128_causal"])
+def test_split_kv_full_workload_sampled_rows(name):
     spec = W.WORKLOADS[name]
     inp = W.make_inputs(spec)
     import attention_forward_sm100_gb300 as pkg
     o, lse = run_lib(inp)   # automatic split count
     q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
-    assert pkg.workspace_bytes(pkg.make_params(q, k, v, causal=False)) > 256   # the automatic count splits
+    # the automatic count splits
+    assert pkg.workspace_bytes(pkg.make_params(q, k, v, causal=spec.causal)) > 256
     rows = W.sample_rows(spec, 128, spec.seed + 100)
     o_ref, l_ref = run_oracle_rows(inp, rows)
     o_gpu, l_gpu = gather_rows(spec, o, lse, rows)

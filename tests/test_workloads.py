@@ -66,6 +66,7 @@ def test_flops_table():
         "varlen_gqa_b8_hq32_hkv8_d128_causal": 1_060_719_804_416,
         "mla_b2_h128_s4096_d128r64_causal": 1_374_725_079_040,
         "fp8_b2_h32_s8192_d128_causal": 1_099_645_845_504,
+        "splitkv_b1_h2_s16384_d128_causal": 137_447_342_080,
     }
     for name, f in expect.items():
         assert W.WORKLOADS[name].flops() == f
@@ -114,6 +115,7 @@ def test_hbm_bytes_table():
         "fp8_b2_h32_s8192_d128_causal": 408_944_640,
         # same with V in e4m3: one byte less per V element
         "fp8qkv_b2_h32_s8192_d128_causal": 408_944_640 - 2 * 8192 * 32 * 128,
+        "splitkv_b1_h2_s16384_d128_causal": 33_685_504,
     }
     for name, n in expect.items():
         assert W.WORKLOADS[name].hbm_bytes() == n
