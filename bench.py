@@ -96,11 +96,12 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def peak_tflops(spec, peaks):
-    """Dense tensor peak for the workload's MMA mix (bf16 burst; FP8 runs at
-    2x the bf16 rate: all-FP8 at 2x, FP8 QK^T with bf16 P.V blended as half
-    the FLOPs at 2x)."""
-    bf16 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+def peak_tflops(spec, peaks, sustained=False):
+    """Dense tensor peak for the workload's MMA mix (bf16 burst, or the
+    sustained bf16 figure; FP8 runs at 2x the bf16 rate: all-FP8 at 2x, FP8
+    QK^T with bf16 P.V blended as half the FLOPs at 2x)."""
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    bf16 = float(peaks.get(key, FALLBACK_PEAKS[key]))
     if spec.v_dtype == "fp8":
         return 2.0 * bf16
     if spec.qk_dtype == "fp8":
@@ -412,7 +413,8 @@ def time_other_workloads(args, dev, stream, peaks, peak_src):
         pkg.check(device=dev)
         clocks = ClockSampler(dev.index if dev.index is not None else 0)
         clocks.start()
-        soak(step, dev, 0.2)        # the same calls keep the clocks up while the sampler starts
+        time.sleep(0.2)             # the sampler starts; the timed calls then run as a burst
+        torch.cuda.synchronize(dev)
         per_call, _ = time_calls(step, args.steps, stream)
         soak(step, dev, 0.6)
         clk = clocks.stop()
@@ -500,21 +502,32 @@ def main():
 
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
-    soak(step, dev, 0.3)            # the same calls keep the clocks up while the sampler starts
+    time.sleep(0.3)                 # the sampler starts; the timed calls then run as a burst
     barrier(world)
     torch.cuda.synchronize(dev)
     per_launch, total_ms = time_calls(step, args.steps, stream)
     # The timed steps last milliseconds, nvidia-smi samples every 100 ms: keep
     # the same load running right after them until a second of samples exists.
+    # These calls are timed too, in batches of 64, for the sustained figure:
+    # the batches of the second half of that second run with the GPU at its
+    # steady power and clock (the timed steps above are a burst from idle).
     t_soak = time.perf_counter()
+    batches = []
     while time.perf_counter() - t_soak < 1.0:
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
         for _ in range(64):
             step()
+        b1.record(stream)
         torch.cuda.synchronize(dev)
+        batches.append((time.perf_counter() - t_soak, b0.elapsed_time(b1) / 64))
     barrier(world)
     clk = clocks.stop()
     pkg.check(device=dev)
     median_ms = statistics.median(per_launch)
+    # steady state: the batches that started after half of the second
+    steady = [ms for t, ms in batches if t >= 0.5] or [ms for _, ms in batches]
+    sus_ms = statistics.median(steady) if steady else None
     total_ms = max_over_ranks(total_ms, world, dev)
     ms = total_ms / args.steps
     flops = spec.flops()
@@ -523,6 +536,15 @@ def main():
     achieved = flops / (kernel_ms * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
     peak = peak_tflops(spec, peaks)
+    sustained = None
+    if sus_ms:
+        sus_peak = peak_tflops(spec, peaks, sustained=True)
+        sus_value = flops / (sus_ms * 1e-3) / 1e12
+        sustained = {"value": sus_value, "unit": "TFLOP/s", "ms_per_step": sus_ms, "peak": sus_peak,
+                     "frac": sus_value / sus_peak, "batches": len(steady),
+                     "peak_source": peak_label(spec, peak_src).replace("burst", "sustained"),
+                     "window": "median of 64-call batches, each timed with CUDA events, that started in "
+                               "the second half of the ~1 s of the same calls run after the timed steps"}
 
     # A problem this small is bound by the host's launch path: also time it
     # through a prepared call and replayed from a CUDA graph.
@@ -625,6 +647,7 @@ def main():
                          "traffic": profiled_traffic(args.workload) if args.pair_cta != "on" else None},
             "kernel_ms": kernel_ms,
             "median_ms": median_ms,
+            "sustained": sustained,
             "clocks": clk,
             "gpu_launches": args.steps * launches_per_step,
             "e2e": e2e,
