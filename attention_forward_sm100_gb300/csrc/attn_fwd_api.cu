@@ -429,6 +429,8 @@ attn_status launch_tc05(const attn_fwd_params* p, cudaStream_t stream) {
   prm.o_stride_b = packed ? 0 : p->o_stride[0];
   prm.o_stride_t = p->o_stride[1];
   prm.o_stride_h = p->o_stride[2];
+  prm.o_store32 = (reinterpret_cast<uintptr_t>(p->o) & 31u) == 0 && (p->o_stride[2] * 2) % 32 == 0 &&
+                  (p->o_stride[1] * 2) % 32 == 0 && (packed || (p->o_stride[0] * 2) % 32 == 0);
   prm.batch = p->batch;
   prm.seqlen_q = p->seqlen_q;
   prm.seqlen_k = p->seqlen_k;

@@ -1023,15 +1023,22 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
 }
 
 // ---------------------------------------------------------------------------------------------
+// 32 columns of one O row (64 bytes) as bf16: two 32-byte stores when O is
+// 32-byte aligned (whole sectors per instruction), else four 16-byte ones.
 template <class T>
-__device__ __forceinline__ void store_row_chunk(uint16_t* dst, const uint32_t (&r)[32], float scale) {
+__device__ __forceinline__ void store_row_chunk(uint16_t* dst, const uint32_t (&r)[32], float scale, bool wide) {
   uint32_t pk[16];
 #pragma unroll
   for (int e = 0; e < 16; ++e)
     pk[e] = ptx::pack_bf16(__uint_as_float(r[2 * e]) * scale, __uint_as_float(r[2 * e + 1]) * scale);
-  uint4* d = reinterpret_cast<uint4*>(dst);
+  if (wide) {
+    ptx::st_global_v8(dst, pk);
+    ptx::st_global_v8(dst + 16, pk + 8);
+  } else {
+    uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-  for (int e = 0; e < 4; ++e) d[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+    for (int e = 0; e < 4; ++e) d[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+  }
 }
 
 // Split-KV: row of the partial O array [split][rows][Hq] (rows = B*Sq, or Tq
@@ -1042,13 +1049,14 @@ __device__ __forceinline__ int64_t partial_row(const Tc05Params& P, const SchedS
   return ((int64_t)s.split * rows + row) * P.heads_q + s.h;
 }
 
-// Split-KV: one 32-column chunk of a row of normalised partial O, in fp32.
+// Split-KV: one 32-column chunk of a row of normalised partial O, in fp32,
+// as four 32-byte stores (partial rows are 32-byte aligned in the workspace).
 __device__ __forceinline__ void store_row_chunk_f32(float* dst, const uint32_t (&r)[32], float scale) {
-  float4* d = reinterpret_cast<float4*>(dst);
+  uint32_t v[32];
 #pragma unroll
-  for (int e = 0; e < 8; ++e)
-    d[e] = make_float4(__uint_as_float(r[4 * e]) * scale, __uint_as_float(r[4 * e + 1]) * scale,
-                       __uint_as_float(r[4 * e + 2]) * scale, __uint_as_float(r[4 * e + 3]) * scale);
+  for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(r[e]) * scale);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) ptx::st_global_v8(dst + 8 * e, v + 8 * e);
 }
 
 template <class T, int CAUSAL>
@@ -1097,7 +1105,7 @@ __device__ void role_correction(const Tc05Params& P, const Ctx& c) {
             uint32_t r[32];
             ptx::tmem_ld32(tO + 32 * q, r);
             ptx::tmem_wait_ld();
-            if (row_valid) store_row_chunk<T>(orow + 32 * q, r, rl);
+            if (row_valid) store_row_chunk<T>(orow + 32 * q, r, rl, P.o_store32 != 0);
           }
         }
       } else if (row_valid && splits_keys<CAUSAL>(P)) {

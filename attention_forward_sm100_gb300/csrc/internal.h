@@ -49,6 +49,7 @@ struct Tc05Params {
   float* lse;
   uint32_t* ws;            // workspace words
   int64_t o_stride_b, o_stride_t, o_stride_h;  // elements
+  int32_t o_store32;       // 1: o and every row stride are 32-byte aligned (256-bit row stores)
   int32_t batch, seqlen_q, seqlen_k, heads_q, heads_kv, group;
   int32_t tiles_per_seq;   // fixed length: ceil(Sq / rows_per_tile)
   int32_t rows_per_tile;   // query rows per work tile (kRowsPerTile, or kRowsPerTilePair for CTA pairs)

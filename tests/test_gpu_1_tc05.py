@@ -181,3 +181,25 @@ def test_strided_views_of_fused_buffers(packed):
     for key, bound in TOL["bf16"].items():
         assert err[key] <= bound, err
     assert bool((out_buf[..., 0, :, :] == 7.0).all())            # the other half is untouched
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dv,splits", [(64, 1), (128, 1), (128, 3)])
+def test_output_rows_only_16_byte_aligned(dv, splits):
+    """O as a view starting 8 elements into rows of Dv + 8 (16-byte aligned,
+    not 32): the epilogue falls back from 32-byte to 16-byte row stores. The
+    result equals, bit for bit, the one written into a contiguous O, and the
+    padding around the view is left alone."""
+    import attention_forward_sm100_gb300 as pkg
+    spec = S(1, 4, 2, 300, 700 if splits > 1 else 300, dv, dv, splits == 1, seed=57)
+    d = W.to_device(W.make_inputs(spec), torch.device("cuda"))
+    kw = dict(causal=spec.causal, softmax_scale=spec.softmax_scale, num_splits=splits)
+    o_ref, l_ref = pkg.forward(d["q"], d["k"], d["v"], **kw)
+    buf = torch.full((1, 300, 4, dv + 8), 3.0, dtype=torch.bfloat16, device="cuda")
+    o = buf[..., 8:]
+    assert (o.data_ptr() % 32) == 16 and (o.stride(2) * 2) % 32 == 16
+    _, lse = pkg.forward(d["q"], d["k"], d["v"], out=o, **kw)
+    pkg.check()
+    assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16))
+    assert torch.equal(lse, l_ref)
+    assert bool((buf[..., :8] == 3.0).all())
