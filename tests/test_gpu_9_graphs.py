@@ -15,6 +15,7 @@ CASES = {
     # name: (spec, num_splits, extra options)
     "bf16_causal_gqa": (W.AttnSpec(2, 8, 2, 700, 700, 128, 128, True, seed=130), 1, {}),
     "split_kv": (W.AttnSpec(1, 4, 2, 256, 3000, 128, 128, False, seed=131), 4, {}),
+    "causal_split_kv": (W.AttnSpec(1, 4, 2, 900, 900, 128, 128, True, seed=137), 3, {}),
     "fp8qkv": (W.AttnSpec(1, 4, 4, 400, 400, 128, 128, True, seed=132, qk_dtype="fp8", v_dtype="fp8"), 1, {}),
     "d64_small": (W.AttnSpec(1, 2, 2, 128, 128, 64, 64, False, seed=133), 1, {}),
     "pairs_causal_gqa": (W.AttnSpec(2, 8, 2, 1100, 1100, 128, 128, True, seed=134), 1, {"pair_cta": "on"}),
