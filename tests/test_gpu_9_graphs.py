@@ -2,8 +2,8 @@
 travel by value in the launch parameters, the workspace counters are reset
 by the kernel itself), so a captured forward can be replayed with new data
 in the same input buffers. Every replay must equal, bit for bit, an eager
-call on the same data; a split-KV call captures both of its kernels, and a
-CTA-pair call its cluster launch."""
+call on the same data; a split-KV call (unmasked or causal) captures both of
+its kernels, and a CTA-pair call its cluster launch."""
 import dataclasses
 
 import pytest
