@@ -415,6 +415,8 @@ def time_other_workloads(args, dev, stream, peaks, peak_src):
         clocks.start()
         time.sleep(0.2)             # the sampler starts; the timed calls then run as a burst
         torch.cuda.synchronize(dev)
+        for _ in range(max(3, args.warmup)):   # warm-up right before the timed calls (clocks up)
+            step()
         per_call, _ = time_calls(step, args.steps, stream)
         soak(step, dev, 0.6)
         clk = clocks.stop()
@@ -505,6 +507,8 @@ def main():
     time.sleep(0.3)                 # the sampler starts; the timed calls then run as a burst
     barrier(world)
     torch.cuda.synchronize(dev)
+    for _ in range(args.warmup):    # the warm-up calls again, right before the timed ones (clocks up)
+        step()
     per_launch, total_ms = time_calls(step, args.steps, stream)
     # The timed steps last milliseconds, nvidia-smi samples every 100 ms: keep
     # the same load running right after them until a second of samples exists.
