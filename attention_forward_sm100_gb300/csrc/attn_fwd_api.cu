@@ -461,7 +461,7 @@ attn_status launch_tc05(const attn_fwd_params* p, cudaStream_t stream) {
   if (grid_for(p, bound) > 0x7fffffffll) return fail(ATTN_ERR_UNSUPPORTED, "too many work tiles for one grid");
   const int grid = (int)grid_for(p, bound);
   prm.schedule = p->schedule;
-  const int mask = p->causal == 0 ? af::kMaskNone : (splits > 1 ? af::kMaskCausalSplit : af::kMaskCausal);
+  const int mask = (p->causal != 0 ? af::kMaskCausal : 0) | (splits > 1 ? af::kMaskNoneSplit : 0);
   cudaError_t e = af::tc05_launch(variant, mask, prm, grid, stream);
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "tcgen05 kernel launch failed: %s", cudaGetErrorString(e));
   if (splits > 1) {

@@ -307,18 +307,17 @@ __device__ __forceinline__ Geo tile_geo(const SchedSlot& s, uint32_t rank) {
   for (int i = 0; i < 2; ++i) {
     g.row[i] = g.q0 + T::MMA_M * i + kBlockM * (int)rank;
     // causal: keys up to the tile's last row, counted from the range's first key
-    const int kv_end = CAUSAL ? min(s.lk, g.q0 + T::MMA_M * (i + 1) - s.koff) : s.lk;
+    const int kv_end = (CAUSAL & kMaskCausal) ? min(s.lk, g.q0 + T::MMA_M * (i + 1) - s.koff) : s.lk;
     g.n[i] = kv_end > 0 ? (kv_end + kBlockN - 1) / kBlockN : 0;
   }
   return g;
 }
 
-// Whether this kernel flavour runs split-KV ranges: the unmasked kernels
-// decide at run time, the causal flavour never (its split code compiles
-// out), the causal split flavour always.
+// Whether this kernel flavour runs split-KV ranges (fixed at compile time;
+// the host launches the split flavours exactly when num_splits > 1).
 template <int CAUSAL>
-__device__ __forceinline__ bool splits_keys(const Tc05Params& P) {
-  return CAUSAL == kMaskCausal ? false : (CAUSAL == kMaskCausalSplit ? true : P.num_splits > 1);
+__device__ __forceinline__ constexpr bool splits_keys(const Tc05Params&) {
+  return (CAUSAL & kMaskNoneSplit) != 0;
 }
 
 // The range's key offset travels only in the causal split flavour (its only user).
@@ -352,7 +351,7 @@ __device__ __forceinline__ SchedSlot decode_work(const Tc05Params& P, int64_t w,
       s.valid = 1; s.b = wt.b; s.h = wt.h; s.t = wt.t; s.split = wt.split;
       if (splits_keys<CAUSAL>(P)) {
         int32_t j0, j1;
-        if (CAUSAL)
+        if (CAUSAL & kMaskCausal)
           causal_split_range(wt.split, P.num_splits, wt.t * P.rows_per_tile, kBlockM, P.rows_per_tile, P.seqlen_k,
                              kBlockN, &j0, &j1);
         else
@@ -413,7 +412,7 @@ __device__ __forceinline__ SchedSlot decode_work(const Tc05Params& P, int64_t w,
         s.split = wt.t % P.num_splits;
         s.t = wt.t / P.num_splits;
         int32_t j0, j1;
-        if (CAUSAL)
+        if (CAUSAL & kMaskCausal)
           causal_split_range(s.split, P.num_splits, s.t * P.rows_per_tile, kBlockM, P.rows_per_tile, ke - ks,
                              kBlockN, &j0, &j1);
         else
@@ -839,7 +838,7 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
     const bool row_valid = qi < s.lq;
     // keys of the range visible to this row (causal: keys 0..qi of the
     // sequence, the range starting at key koff of it)
-    const int lim = CAUSAL ? min(s.lk, qi + 1 - s.koff) : s.lk;
+    const int lim = (CAUSAL & kMaskCausal) ? min(s.lk, qi + 1 - s.koff) : s.lk;
     const int first_row = g.row[i];
     // LSE element: [B][Hq][Sq] (or [Hq][Tq] packed); a split-KV range writes
     // its partial LSE to copy `split` of that layout, [split][B][Hq][Sq] (or
@@ -901,7 +900,7 @@ __device__ void role_softmax(const Tc05Params& P, const Ctx& c, const int i) {
           sv[2 * e + 1] = a1;
         }
       }
-      const bool need_mask = (kb + kBlockN > s.lk) || (CAUSAL && s.koff + kb + kBlockN - 1 > first_row);
+      const bool need_mask = (kb + kBlockN > s.lk) || ((CAUSAL & kMaskCausal) && s.koff + kb + kBlockN - 1 > first_row);
       if (need_mask) {
         const int vis = lim - kb;
         if constexpr (T::V8) {
@@ -1329,6 +1328,7 @@ template <class T>
 cudaError_t tc05_launch_t(int mask, const Tc05Params& prm, int grid, cudaStream_t stream) {
   if (mask == kMaskNone) return tc05_launch_tc<T, kMaskNone>(prm, grid, stream);
   if (mask == kMaskCausal) return tc05_launch_tc<T, kMaskCausal>(prm, grid, stream);
+  if (mask == kMaskNoneSplit) return tc05_launch_tc<T, kMaskNoneSplit>(prm, grid, stream);
   if constexpr (!T::PAIR) {
     if (mask == kMaskCausalSplit) return tc05_launch_tc<T, kMaskCausalSplit>(prm, grid, stream);
   }

@@ -105,10 +105,11 @@ attn_status report_error(attn_status st, const char* fmt, ...);
 
 // Static configuration of a variant (host).
 Tc05Config tc05_config(int variant);
-// Mask flavours of the tcgen05 kernel: no mask (split-KV decided at run
-// time), causal without split-KV (its split code compiled out), causal with
-// split-KV (pair variants have none).
-enum Tc05Mask : int { kMaskNone = 0, kMaskCausal = 1, kMaskCausalSplit = 2 };
+// Flavours of the tcgen05 kernel, two bits: causal mask (1) and split-KV
+// (2), so that a kernel carries only the code its calls run (the split
+// partial stores, for one, are compiled out of the unsplit flavours). Pair
+// variants have no causal split flavour.
+enum Tc05Mask : int { kMaskNone = 0, kMaskCausal = 1, kMaskNoneSplit = 2, kMaskCausalSplit = 3 };
 // Launch of one variant (defined in the per-variant translation units); a
 // pair variant's grid counts CTAs and must be even.
 cudaError_t tc05_launch(int variant, int mask, const Tc05Params& prm, int grid, cudaStream_t stream);
