@@ -292,8 +292,8 @@ def forward(q, k, v, *, causal=False, softmax_scale=None, q_rope=None, k_rope=No
     parts q_rope [..,Hq,R] and k_rope [..,R] (one per token, shared by heads);
     fp8 e4m3 q/k need per-token fp32 scales q_scale [B,Hq,Sq] / [Hq,Tq] and
     k_scale [B,Hkv,Sk] / [Hkv,Tk]. ``num_splits``: split-KV key ranges per
-    query tile (0 = the library's choice, 1 = off; unmasked fixed-length
-    problems only). ``schedule``: "dynamic" (default), "static" or "grid",
+    query tile (0 = the library's choice, 1 = off; masked or not, fixed
+    length or packed; not with causal CTA pairs). ``schedule``: "dynamic" (default), "static" or "grid",
     how work tiles reach CTAs (results are identical). ``pair_cta``: "auto"
     (the library's choice), "off", or "on": two CTAs of a cluster share every
     MMA (bf16, Dqk = Dv = 128, rope 0 or 64). Asynchronous on ``stream``
