@@ -4,8 +4,9 @@ merged result is compared with the oracle (which never splits) on shapes that
 span several key tiles with ragged ends, for every kernel variant, for
 explicit and automatic split counts, unmasked and under the causal mask
 (ranges cut from the keys each query tile sees, some of them empty), and at
-full size on sampled rows: the short-query / long-key workload and one long
-causal sequence with a single head."""
+full size on sampled rows: the short-query / long-key workload, the long
+causal workload (one 16k-token sequence, two heads) and one causal sequence
+of 8192 tokens with a single head."""
 import pytest
 import torch
 
