@@ -544,3 +544,34 @@ def test_pair_schedule_packed(pkg):
     order = pkg.schedule(p, host_cu_seqlens_q=cu)
     expect = {(b, h, t) for b, n in enumerate(lens) for h in range(32) for t in range((n + 511) // 512)}
     assert len(order) == len(expect) and set(order) == expect
+
+
+def test_causal_ranges_keep_the_kernel_protocol(pkg):
+    """The kernel's per-range key-tile counts (tile geometry: MMA tile i of a
+    work tile visits ceil(min(range keys, q0 + 128 (i + 1) - range start) /
+    128) tiles of the range) must satisfy what its barrier protocol assumes:
+    the first MMA tile visits no more tiles than the second, and at least one
+    whenever the second visits any; and every row of a visiting MMA tile sees
+    the range's first key (a fully masked first tile would leave the running
+    max at -inf)."""
+    n_checked = 0
+    for sq in (1, 128, 129, 256, 257, 600, 1000, 4096):
+        for sk in (1, 100, 128, 129, 300, 1000, 4096):
+            for splits in (2, 3, 5, 9, 64):
+                p = _split_params(pkg, B=1, Sq=sq, Sk=sk, Hq=1, Hkv=1, causal=True, splits=splits)
+                n = pkg.plan(p).num_splits
+                for t in range((sq + 255) // 256):
+                    q0 = 256 * t
+                    for r in range(n):
+                        b, e = pkg.key_range(p, t, r, sk)
+                        counts = []
+                        for i in range(2):
+                            kv_end = min(e - b, q0 + 128 * (i + 1) - b)
+                            counts.append((kv_end + 127) // 128 if kv_end > 0 else 0)
+                        assert counts[0] <= counts[1], (sq, sk, splits, t, r, counts)
+                        assert counts[1] == 0 or counts[0] >= 1, (sq, sk, splits, t, r, counts)
+                        for i in range(2):
+                            if counts[i]:
+                                assert q0 + 128 * i >= b, (sq, sk, splits, t, r, i)
+                        n_checked += 1
+    assert n_checked > 1000
