@@ -7,6 +7,7 @@ call. There is no CPU path.
 """
 from __future__ import annotations
 
+import collections
 import ctypes
 import os
 import threading
@@ -132,6 +133,20 @@ def default_workspace(device, nbytes: int = WORKSPACE_BYTES) -> torch.Tensor:
             ws = torch.zeros(max(nbytes, WORKSPACE_BYTES), dtype=torch.uint8, device=device)
             _workspaces[key] = ws
         return ws
+
+
+# forward(): validated, marshalled parameters of recent calls, keyed by every
+# tensor's pointer, shape, strides and dtype and by the options, so that a
+# repeated call skips the Python-side checks and struct filling. A key fixes
+# the struct up to the output / LSE buffers forward() allocates (fresh,
+# contiguous, same shapes) and the workspace, which are set per call.
+_PARAMS_CACHE_SIZE = 64
+_params_cache = collections.OrderedDict()
+_params_cache_lock = threading.Lock()
+
+
+def _tensor_key(t):
+    return None if t is None else (t.data_ptr(), tuple(t.shape), t.stride(), t.dtype)
 
 
 def workspace_bytes(p: Params) -> int:
@@ -299,28 +314,57 @@ def forward(q, k, v, *, causal=False, softmax_scale=None, q_rope=None, k_rope=No
     MMA (bf16, Dqk = Dv = 128, rope 0 or 64). Asynchronous on ``stream``
     (default: the current torch stream).
     """
-    for name, t in (("q", q), ("k", k), ("v", v), ("q_rope", q_rope), ("k_rope", k_rope), ("q_scale", q_scale),
-                    ("k_scale", k_scale), ("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k),
-                    ("cu_seqlens_v", cu_seqlens_v)):
-        _require_cuda(name, t)
     L = lib()
     packed = cu_seqlens_q is not None
     dev = q.device
-    if out is None:
+    own_out, own_lse = out is None, lse is None and return_lse
+    key = None
+    if workspace is None:
+        key = (dev.type, dev.index, _tensor_key(q), _tensor_key(k), _tensor_key(v), _tensor_key(q_rope),
+               _tensor_key(k_rope), _tensor_key(q_scale), _tensor_key(k_scale), _tensor_key(cu_seqlens_q),
+               _tensor_key(cu_seqlens_k), _tensor_key(cu_seqlens_v), _tensor_key(out), _tensor_key(lse),
+               return_lse, bool(causal), softmax_scale, max_seqlen_q, max_seqlen_k, backend, num_splits, schedule,
+               pair_cta)
+        with _params_cache_lock:
+            hit = _params_cache.get(key)
+            if hit is not None:
+                _params_cache.move_to_end(key)
+    else:
+        hit = None
+    if hit is None:
+        for name, t in (("q", q), ("k", k), ("v", v), ("q_rope", q_rope), ("k_rope", k_rope), ("q_scale", q_scale),
+                        ("k_scale", k_scale), ("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k),
+                        ("cu_seqlens_v", cu_seqlens_v), ("out", out), ("lse", lse)):
+            _require_cuda(name, t)
+    if own_out:
         out = torch.empty(q.shape[:-1] + (head_dim_v(v),), dtype=torch.bfloat16, device=dev)
-    if lse is None and return_lse:
+    if own_lse:
         if packed:
             lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=dev)
         else:
             lse = torch.empty((q.shape[0], q.shape[2], q.shape[1]), dtype=torch.float32, device=dev)
-    p = make_params(q, k, v, causal=causal, softmax_scale=softmax_scale, q_rope=q_rope, k_rope=k_rope,
-                    q_scale=q_scale, k_scale=k_scale, cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k,
-                    max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k, out=out, lse=lse,
-                    workspace=workspace, backend=backend, num_splits=num_splits, schedule=schedule,
-                    pair_cta=pair_cta, cu_seqlens_v=cu_seqlens_v)
+    if hit is not None:
+        p = Params.from_buffer_copy(hit[0])
+        need = hit[1]
+        if own_out:
+            p.o = out.data_ptr()
+        if own_lse:
+            p.lse = lse.data_ptr()
+    else:
+        p = make_params(q, k, v, causal=causal, softmax_scale=softmax_scale, q_rope=q_rope, k_rope=k_rope,
+                        q_scale=q_scale, k_scale=k_scale, cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k,
+                        max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k, out=out, lse=lse,
+                        workspace=workspace, backend=backend, num_splits=num_splits, schedule=schedule,
+                        pair_cta=pair_cta, cu_seqlens_v=cu_seqlens_v)
+        need = 0
+        if workspace is None:
+            with torch.cuda.device(dev):
+                need = workspace_bytes(p)
+            with _params_cache_lock:
+                _params_cache[key] = (Params.from_buffer_copy(p), need)
+                while len(_params_cache) > _PARAMS_CACHE_SIZE:
+                    _params_cache.popitem(last=False)
     if workspace is None:
-        with torch.cuda.device(dev):
-            need = workspace_bytes(p)
         workspace = default_workspace(dev, need)
         p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel()
     if stream is None:
