@@ -312,7 +312,9 @@ def forward(q, k, v, *, causal=False, softmax_scale=None, q_rope=None, k_rope=No
     how work tiles reach CTAs (results are identical). ``pair_cta``: "auto"
     (the library's choice), "off", or "on": two CTAs of a cluster share every
     MMA (bf16, Dqk = Dv = 128, rope 0 or 64). Asynchronous on ``stream``
-    (default: the current torch stream).
+    (default: the current torch stream). A call with the same tensors
+    (pointer, shape, strides, dtype) and options as a recent one reuses its
+    validated parameters.
     """
     L = lib()
     packed = cu_seqlens_q is not None
