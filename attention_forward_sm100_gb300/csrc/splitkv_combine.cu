@@ -22,9 +22,10 @@ namespace af {
 namespace {
 
 constexpr int kCombineWarps = 8;
-constexpr int kBatch = 8;   // partial rows each lane loads before accumulating
 
-template <int DV>
+// kBatch: partial rows each lane loads before accumulating (4 for up to four
+// ranges, so that fewer registers leave room for more warps; 8 otherwise)
+template <int DV, int kBatch>
 __global__ void __launch_bounds__(kCombineWarps * 32) splitkv_combine_kernel(const SplitCombineParams p) {
   constexpr int C = DV / 32;   // output columns per lane
   const int lane = threadIdx.x & 31;
@@ -124,12 +125,16 @@ cudaError_t splitkv_combine_launch(const SplitCombineParams& p, int head_dim_v, 
   if (rows == 0) return cudaSuccess;
   const int64_t blocks = (rows + kCombineWarps - 1) / kCombineWarps;
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
-  if (head_dim_v == 128)
-    splitkv_combine_kernel<128><<<(unsigned)blocks, kCombineWarps * 32, 0, stream>>>(p);
-  else if (head_dim_v == 64)
-    splitkv_combine_kernel<64><<<(unsigned)blocks, kCombineWarps * 32, 0, stream>>>(p);
-  else
+  const bool few = p.splits <= 4;
+  if (head_dim_v == 128) {
+    if (few) splitkv_combine_kernel<128, 4><<<(unsigned)blocks, kCombineWarps * 32, 0, stream>>>(p);
+    else splitkv_combine_kernel<128, 8><<<(unsigned)blocks, kCombineWarps * 32, 0, stream>>>(p);
+  } else if (head_dim_v == 64) {
+    if (few) splitkv_combine_kernel<64, 4><<<(unsigned)blocks, kCombineWarps * 32, 0, stream>>>(p);
+    else splitkv_combine_kernel<64, 8><<<(unsigned)blocks, kCombineWarps * 32, 0, stream>>>(p);
+  } else {
     return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 
