@@ -28,6 +28,9 @@ constexpr int kCombineWarps = 8;
 template <int DV, int kBatch>
 __global__ void __launch_bounds__(kCombineWarps * 32) splitkv_combine_kernel(const SplitCombineParams p) {
   constexpr int C = DV / 32;   // output columns per lane
+  // Launched as a programmatic dependent of the attention kernel: wait until
+  // that grid has completed and its partial results are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   // (query row, head) pairs, head fastest; query rows are (b, i) or packed t
   const int64_t row = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
@@ -126,15 +129,27 @@ cudaError_t splitkv_combine_launch(const SplitCombineParams& p, int head_dim_v, 
   const int64_t blocks = (rows + kCombineWarps - 1) / kCombineWarps;
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
   const bool few = p.splits <= 4;
-  if (head_dim_v == 128) {
-    if (few) splitkv_combine_kernel<128, 4><<<(unsigned)blocks, kCombineWarps * 32, 0, stream>>>(p);
-    else splitkv_combine_kernel<128, 8><<<(unsigned)blocks, kCombineWarps * 32, 0, stream>>>(p);
-  } else if (head_dim_v == 64) {
-    if (few) splitkv_combine_kernel<64, 4><<<(unsigned)blocks, kCombineWarps * 32, 0, stream>>>(p);
-    else splitkv_combine_kernel<64, 8><<<(unsigned)blocks, kCombineWarps * 32, 0, stream>>>(p);
-  } else {
+  void (*kern)(const SplitCombineParams) = nullptr;
+  if (head_dim_v == 128)
+    kern = few ? splitkv_combine_kernel<128, 4> : splitkv_combine_kernel<128, 8>;
+  else if (head_dim_v == 64)
+    kern = few ? splitkv_combine_kernel<64, 4> : splitkv_combine_kernel<64, 8>;
+  else
     return cudaErrorInvalidValue;
-  }
+  // Programmatic dependent launch: the merge's blocks may start while the
+  // attention kernel's last CTAs finish (each waits at griddepcontrol.wait).
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kCombineWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
