@@ -461,6 +461,11 @@ attn_status launch_tc05(const attn_fwd_params* p, cudaStream_t stream) {
   if (grid_for(p, bound) > 0x7fffffffll) return fail(ATTN_ERR_UNSUPPORTED, "too many work tiles for one grid");
   const int grid = (int)grid_for(p, bound);
   prm.schedule = p->schedule;
+  // Calls with fewer CTAs than SMs are dominated by launch latency: their
+  // set-up overlaps the previous kernel (programmatic dependent launch; bf16
+  // variants, which wait for that kernel before any global access). A full
+  // grid gains nothing from it.
+  prm.dependent_launch = (p->qk_dtype == ATTN_DTYPE_BF16 && grid < sm_count_cached()) ? 1 : 0;
   const int mask = (p->causal != 0 ? af::kMaskCausal : 0) | (splits > 1 ? af::kMaskNoneSplit : 0);
   cudaError_t e = af::tc05_launch(variant, mask, prm, grid, stream);
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "tcgen05 kernel launch failed: %s", cudaGetErrorString(e));

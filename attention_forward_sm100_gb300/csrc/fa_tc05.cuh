@@ -1154,6 +1154,7 @@ __global__ void __launch_bounds__(512, 1) fa_tc05_kernel(const __grid_constant__
   c.rank = T::PAIR ? ptx::cluster_ctarank() : 0u;
   c.peer_abort = 0u;
   if (c.sbase & 1023u) {  // the swizzled tiles need a 1024-byte aligned base (same in both CTAs of a pair)
+    if constexpr (!T::FP8) ptx::grid_dependency_wait();
     if (threadIdx.x == 0) atomicCAS(&P.ws[kWsErrorCode], 0u, 2u);
     return;
   }
@@ -1223,6 +1224,13 @@ __global__ void __launch_bounds__(512, 1) fa_tc05_kernel(const __grid_constant__
   ptx::tc_fence_after();
   c.tmem = *reinterpret_cast<volatile uint32_t*>(smem + T::OFF_TMEM_SLOT);
   if constexpr (T::PAIR) c.peer_abort = ptx::mapa(c.sbase + T::OFF_ABORT, c.rank ^ 1u);
+  // The set-up above touches no global memory, so it may overlap the
+  // previous kernel on the stream (programmatic dependent launch); from here
+  // on the kernel reads inputs and writes outputs and the workspace, so it
+  // waits until that kernel has completed and its writes are visible. (The
+  // FP8 variants are never launched that way: any added code in them
+  // measured ~1 % slower, their softmax being at its register ceiling.)
+  if constexpr (!T::FP8) ptx::grid_dependency_wait();   // returns at once without a dependency
 
   const int wg = warp >> 2;
   if (wg < 2) {
@@ -1317,8 +1325,23 @@ cudaError_t tc05_launch_tc(const Tc05Params& prm, int grid, cudaStream_t stream)
       const cudaLaunchConfig_t cfg = pair_config<T>(grid, stream, attr);
       const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm);
       if (e != cudaSuccess) return e;
-    } else {
+    } else if (T::FP8 || !prm.dependent_launch) {
       kern<<<grid, 512, T::SMEM_BYTES, stream>>>(prm);
+    } else {
+      // programmatic dependent launch: set-up overlaps the previous kernel's
+      // last CTAs (the kernel waits before its first global access)
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)grid);
+      cfg.blockDim = dim3(512);
+      cfg.dynamicSmemBytes = T::SMEM_BYTES;
+      cfg.stream = stream;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm);
+      if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
   });

@@ -62,6 +62,7 @@ struct Tc05Params {
   uint64_t timeout_ns;     // limit of every device wait
   int32_t withhold_v;      // testing: block 0 skips its first V tile load
   int32_t schedule;        // attn_schedule: how the producer advances to its next work index
+  int32_t dependent_launch; // host only: launch as a programmatic dependent of the previous kernel
   int32_t num_splits;      // key ranges per query tile (1: no split-KV)
   int32_t kv_tiles;        // split-KV: ceil(seqlen_k / kBlockN)
   float* lse_part;         // split-KV: partial LSE [splits][B][Hq][Sq] / [splits][Hq][Tq]

@@ -112,6 +112,10 @@ __device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* v) {
                : "memory");
 }
 
+// Waits until the grid this one programmatically depends on has completed
+// and its memory is visible (returns at once without such a dependency).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, uint32_t bar, int c0, int c1, int c2,
                                             int c3) {
   asm volatile(

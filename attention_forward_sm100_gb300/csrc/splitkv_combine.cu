@@ -17,6 +17,7 @@
 #include <math.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace af {
 namespace {
@@ -30,7 +31,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) splitkv_combine_kernel(con
   constexpr int C = DV / 32;   // output columns per lane
   // Launched as a programmatic dependent of the attention kernel: wait until
   // that grid has completed and its partial results are visible.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  ptx::grid_dependency_wait();
   const int lane = threadIdx.x & 31;
   // (query row, head) pairs, head fastest; query rows are (b, i) or packed t
   const int64_t row = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
